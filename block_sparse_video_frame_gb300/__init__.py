@@ -1,0 +1,276 @@
+"""Python binding of libvdit (frame-window + reference-frame block-sparse attention
+for sm_103a). Argument marshalling only: every step runs in the library's CUDA
+kernels; torch provides device memory and the current stream.
+
+The library must be built first (``__graft_entry__.build()`` or
+``python -m block_sparse_video_frame_gb300._build``). If it is missing, every
+call raises: there is no CPU or eager fallback.
+
+    plan = attn_plan(F, T, W, ref, block_size)          # "Deleting the Mask", Fig. 3
+    st = key_stats(q, k, scale)                          # "Unchaining the Softmax"
+    o, lse = attn_fwd(plan, q, k, v, st, scale)          # fused tcgen05 kernel
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import configs  # noqa: F401  (plain data, importable without the library)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvdit.so")
+
+VDIT_OK, VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA, VDIT_ERR_NOMEM, VDIT_ERR_TIMEOUT = range(6)
+MODES = {"auto": 0, "online": 1, "static": 2}
+EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_plan_status",
+            "vdit_plan_destroy", "vdit_key_stats_workspace_size", "vdit_key_stats",
+            "vdit_attn_fwd", "vdit_last_error", "vdit_version")
+
+
+class VditError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"libvdit status {status}: {msg}")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_frames", ctypes.c_int32), ("tokens_per_frame", ctypes.c_int32),
+                ("window_radius", ctypes.c_int32), ("ref_frame", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("dense", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int64), ("n_qblocks", ctypes.c_int32),
+                ("nnz", ctypes.c_int64), ("live_pairs", ctypes.c_int64),
+                ("n_segments", ctypes.c_int32), ("n_units", ctypes.c_int32),
+                ("n_classes", ctypes.c_int32),
+                ("d_row_ptr", ctypes.c_void_p), ("d_col_idx", ctypes.c_void_p),
+                ("d_frame_runs", ctypes.c_void_p), ("d_segments", ctypes.c_void_p),
+                ("d_units", ctypes.c_void_p), ("d_class_off", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+_I64x3 = ctypes.c_int64 * 3
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libvdit.so and declare its C signatures. Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libvdit is not built ({path} missing): run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        lib.vdit_attn_plan.argtypes = [i32, i32, i32, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.vdit_plan_rebuild.argtypes = [vp, vp]
+        lib.vdit_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        lib.vdit_plan_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        lib.vdit_plan_destroy.argtypes = [vp]
+        lib.vdit_plan_destroy.restype = None
+        lib.vdit_key_stats_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.vdit_key_stats_workspace_size.restype = ctypes.c_size_t
+        lib.vdit_key_stats.argtypes = [vp, vp, i32, i32, i32, i32, _I64x3, _I64x3, f32, f32,
+                                       vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.vdit_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, _I64x3, _I64x3,
+                                      _I64x3, _I64x3, f32, vp, vp, vp, i32, vp]
+        for fn in ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info",
+                   "vdit_plan_status", "vdit_key_stats", "vdit_attn_fwd"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.vdit_last_error.restype = ctypes.c_char_p
+        lib.vdit_last_error.argtypes = []
+        lib.vdit_version.restype = ctypes.c_char_p
+        lib.vdit_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(status):
+    if status != VDIT_OK:
+        raise VditError(status, load_library().vdit_last_error().decode())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _strides(t):
+    return _I64x3(*[int(s) for s in t.stride()[:3]])
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check_bhnd(name, t, D=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dim() != 4:
+        raise ValueError(f"{name} must be a 4-D [B, H, N, D] tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have a contiguous last dimension")
+    if D is not None and t.shape[3] != D:
+        raise ValueError(f"{name} head dim {t.shape[3]} != {D}")
+
+
+class Plan:
+    """Owns a vdit_plan (device block schedule + work units)."""
+
+    def __init__(self, F, T, W, ref, block_size, stream=None):
+        lib = load_library()
+        h = ctypes.c_void_p()
+        _check(lib.vdit_attn_plan(int(F), int(T), int(W), int(ref), int(block_size),
+                                  _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self.info = PlanInfo()
+        _check(lib.vdit_plan_get_info(h, ctypes.byref(self.info)))
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def num_tokens(self):
+        return int(self.info.num_tokens)
+
+    @property
+    def live_pairs(self):
+        return int(self.info.live_pairs)
+
+    def rebuild(self, stream=None):
+        _check(load_library().vdit_plan_rebuild(self._h, _stream(stream)))
+
+    def status(self, stream=None) -> int:
+        code = ctypes.c_int32()
+        st = load_library().vdit_plan_status(self._h, _stream(stream), ctypes.byref(code))
+        if st not in (VDIT_OK, VDIT_ERR_TIMEOUT):
+            _check(st)
+        return int(code.value)
+
+    def _device_array(self, ptr, n):
+        """Copy of n int32 values of plan-owned device memory (zero-copy view via
+        __cuda_array_interface__, then clone)."""
+        import torch
+        if not n:
+            return torch.empty(0, dtype=torch.int32, device="cuda")
+        view = torch.as_tensor(_DeviceInts(ptr, int(n)), device="cuda")
+        return view.clone()
+
+    def row_ptr(self):
+        return self._device_array(self.info.d_row_ptr, self.info.n_qblocks + 1)
+
+    def col_idx(self):
+        return self._device_array(self.info.d_col_idx, self.info.nnz)
+
+    def frame_runs(self):
+        return self._device_array(self.info.d_frame_runs, 4 * self.info.num_frames).view(-1, 4)
+
+    def segments(self):
+        return self._device_array(self.info.d_segments, 8 * self.info.n_segments).view(-1, 8)
+
+    def units(self):
+        return self._device_array(self.info.d_units, self.info.n_units)
+
+    def class_offsets(self):
+        return self._device_array(self.info.d_class_off, self.info.n_classes + 1)
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            load_library().vdit_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _DeviceInts:
+    """Describes plan-owned int32 device memory to torch (no copy, no ownership)."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4",
+                                         "data": (int(ptr), True), "version": 3,
+                                         "strides": None}
+
+
+def attn_plan(F, T, W, ref, block_size, stream=None) -> Plan:
+    """Block schedule of the frame-window + reference-frame mask (vdit_attn_plan)."""
+    return Plan(F, T, W, ref, block_size, stream)
+
+
+def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None):
+    """Per-head key mean, max centred key norm, max query norm, gap bound G and
+    eligibility G <= tau (vdit_key_stats). Returns a dict of CUDA tensors."""
+    import torch
+    _check_bhnd("q", q)
+    _check_bhnd("k", k, q.shape[3])
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16:
+        raise ValueError("q and k must be bf16")
+    if q.shape != k.shape:
+        raise ValueError("q and k must have the same shape")
+    B, H, N, D = q.shape
+    lib = load_library()
+    dev = q.device
+    out = dict(k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev),
+               k_rmax=torch.empty((B, H), dtype=torch.float32, device=dev),
+               q_nmax=torch.empty((B, H), dtype=torch.float32, device=dev),
+               gap=torch.empty((B, H), dtype=torch.float32, device=dev),
+               eligible=torch.empty((B, H), dtype=torch.uint8, device=dev))
+    need = lib.vdit_key_stats_workspace_size(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
+    _check(lib.vdit_key_stats(_ptr(q), _ptr(k), B, H, N, D, _strides(q), _strides(k),
+                              float(scale), float(tau), _ptr(out["k_mean"]), _ptr(out["k_rmax"]),
+                              _ptr(out["q_nmax"]), _ptr(out["gap"]), _ptr(out["eligible"]),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream)))
+    return out
+
+
+def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype=None,
+             with_lse=True, out=None, lse=None, stream=None):
+    """Fused block-sparse attention (vdit_attn_fwd). Returns (o, lse or None)."""
+    import torch
+    _check_bhnd("q", q)
+    D = q.shape[3]
+    _check_bhnd("k", k, D)
+    _check_bhnd("v", v, D)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bf16")
+        if t.shape != q.shape:
+            raise ValueError(f"{name} shape {tuple(t.shape)} != q shape {tuple(q.shape)}")
+    B, H, N, _ = q.shape
+    if N != plan.num_tokens:
+        raise ValueError(f"sequence length {N} != plan's num_tokens {plan.num_tokens}")
+    if scale is None:
+        scale = D ** -0.5
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=out_dtype or torch.bfloat16, device=q.device)
+    _check_bhnd("out", out, D)
+    o_code = {torch.bfloat16: 0, torch.float32: 1}[out.dtype]
+    if with_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None and not (lse.is_contiguous() and lse.dtype == torch.float32
+                                and tuple(lse.shape) == (B, H, N)):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    km = kr = el = None
+    if stats is not None:
+        km, kr, el = stats["k_mean"], stats["k_rmax"], stats["eligible"]
+    _check(load_library().vdit_attn_fwd(
+        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), o_code, _ptr(lse), B, H, D,
+        _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
+        _ptr(el), m, _stream(stream)))
+    return out, lse
+
+
+def version() -> str:
+    return load_library().vdit_version().decode()

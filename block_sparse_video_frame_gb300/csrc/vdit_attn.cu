@@ -1,0 +1,701 @@
+// Fused frame-window + reference-frame block-sparse attention for sm_103a.
+//
+// "HeyGen x Google Cloud: Bringing Avatar IV to TPUs":
+//   "Deleting the Mask" (Fig. 3) -- the live key set of a query frame is at
+//     most two runs of whole frames (the window and the reference frame), so
+//     every key tile is fully live: no mask predicate, no padding, one pass.
+//   "Unchaining the Softmax" (Fig. 4) -- on eligible heads each row's max is
+//     fixed up front to m_i = scale * (q_i . c + |q_i| R) (Cauchy-Schwarz on
+//     mean-centred keys), so p = 2^(s*log2e - m~) needs no running max and no
+//     rescale of the accumulator; other heads run online softmax in the same
+//     kernel (head-uniform branch).
+//   "Proving the Pixels Didn't Change" -- P is rounded to bf16 and the final
+//     P.V product runs on the matrix unit.
+//
+// GB300 design. Persistent grid (one CTA per SM, 320 threads):
+//   warps 0-3, 4-7  softmax warpgroups, one per 128-row query tile; thread t
+//                   of a warpgroup owns TMEM lane t = query row t
+//   warp 8          TMA producer: Q tiles, then a 2-stage ring of K and V
+//                   tiles (128 keys x D, bf16, 128-byte swizzle)
+//   warp 9          TMEM allocator and single-thread tcgen05.mma issuer
+// A work unit is (b, h, segment, pair of query tiles). Both tiles of a unit
+// lie in one segment (frames with identical key runs), share every K/V tile
+// and ping-pong on the tensor core:
+//   S0 = Q0 K_0^T, S1 = Q1 K_0^T, then for each key tile j:
+//   O0 += P0_j V_j, S0 = Q0 K_{j+1}^T, O1 += P1_j V_j, S1 = Q1 K_{j+1}^T
+// so one warpgroup's exponentials overlap the other's MMAs. TMEM (512 cols):
+// O0 | O1 | S0 | S1; P (bf16, two per 32-bit column) overwrites the first half
+// of its S buffer and is the A operand (from TMEM) of the P.V MMA.
+// Every wait is bounded in time; on expiry the CTA records a site code in the
+// plan's status word, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "vdit_internal.h"
+#include "vdit_ptx.cuh"
+
+namespace vdit {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBK = 128;              // keys per K/V tile
+constexpr int kStages = 2;            // K and V ring depth
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kHalfBytes = 128 * 128; // 128 rows x 64 bf16 (one swizzle-atom column)
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+constexpr float kLazyRescale = 8.0f;  // online: rescale only when the max rises > 2^8
+
+// status-word site codes (which wait expired)
+enum : int {
+    kSiteQfree = 1, kSiteKfree, kSiteVfree, kSiteQfullMma, kSiteKfull, kSiteVfull, kSitePfull,
+    kSiteOfree, kSiteQfullSm, kSiteSfull, kSiteOfull, kSiteDrain
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kTileBytes = kTileRows * D * 2;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTilesPerUnit * kTileBytes;
+    static constexpr int kV = kK + kStages * kTileBytes;
+    static constexpr int kBar = kV + kStages * kTileBytes;
+    static constexpr int kBytes = kBar + 256;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+    static constexpr uint32_t kTmemO = 0;         // O0 at col 0, O1 at col D
+    static constexpr uint32_t kTmemS = 2 * D;     // S0 at 2D, S1 at 2D + 128
+};
+
+// barrier slots (8 bytes each) after the tiles
+enum : int {
+    kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = 4, kBarVfull = 6, kBarVfree = 8,
+    kBarSfull = 10, kBarPfull = 12, kBarOfull = 14, kBarOfree = 16, kBarFinal = 18,
+    kNumBars = 19
+};
+
+struct Params {
+    const int32_t *segments, *units, *class_off;
+    int n_classes;
+    int B, H, N;
+    long long total_work;
+    void *o;
+    long long os0, os1, os2;
+    int o_f32;
+    float *lse;
+    float scale_log2;  // scale * log2(e)
+    const float *k_mean, *k_rmax;
+    const uint8_t *elig;
+    int mode;
+    int *status;
+    unsigned long long timeout_ns;
+};
+
+struct Work {
+    int b, h, bh;
+    int row0, rows;        // segment rows
+    int lo0, hi0, lo1, hi1;
+    int pair, ntile;       // this unit's tile pair, tiles in the segment
+    int nact;              // active query tiles (1 or 2)
+    int nt0, nkt;          // key tiles of run 0, total key tiles
+};
+
+__device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
+    const int BH = p.B * p.H;
+    long long base = 0;
+    int c = 0, n_c = 0;
+    for (c = 0; c < p.n_classes; ++c) {
+        n_c = p.class_off[c + 1] - p.class_off[c];
+        const long long span = (long long)n_c * BH;
+        if (w < base + span) break;
+        base += span;
+    }
+    const long long local = w - base;
+    u.bh = (int)(local / n_c);
+    const int ui = p.class_off[c] + (int)(local % n_c);
+    u.b = u.bh / p.H;
+    u.h = u.bh % p.H;
+    const int code = p.units[ui];
+    const int32_t *s = p.segments + kSegInts * (code >> 16);
+    u.pair = code & 0xFFFF;
+    u.row0 = s[0]; u.rows = s[1];
+    u.lo0 = s[2]; u.hi0 = s[3]; u.lo1 = s[4]; u.hi1 = s[5];
+    u.ntile = s[6];
+    u.nact = min(kTilesPerUnit, u.ntile - kTilesPerUnit * u.pair);
+    u.nt0 = (u.hi0 - u.lo0 + kBK - 1) / kBK;
+    u.nkt = u.nt0 + (u.hi1 - u.lo1 + kBK - 1) / kBK;
+}
+
+// first row of query tile q of the unit (last tile of a segment ends at its end)
+__device__ __forceinline__ int tile_row(const Work &u, int q) {
+    const int t = kTilesPerUnit * u.pair + q;
+    const int off = min(t * kTileRows, max(u.rows - kTileRows, 0));
+    return u.row0 + off;
+}
+
+// key tile j: first key and number of live keys
+__device__ __forceinline__ void key_tile(const Work &u, int j, int &start, int &nvalid) {
+    if (j < u.nt0) {
+        start = u.lo0 + j * kBK;
+        nvalid = min(kBK, u.hi0 - start);
+    } else {
+        start = u.lo1 + (j - u.nt0) * kBK;
+        nvalid = min(kBK, u.hi1 - start);
+    }
+}
+
+// Wait that ignores the abort flag, used only to drain in-flight copies/MMAs.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bar0 = sbase + L::kBar;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBar + 8 * kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBar + 8 * kNumBars + 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint64_t tlim = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kBarQfull), 1);
+        mbar_init(bar(kBarQfree), 1 + 8);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarKfull + s), 1);
+            mbar_init(bar(kBarKfree + s), 1);
+            mbar_init(bar(kBarVfull + s), 1);
+            mbar_init(bar(kBarVfree + s), 1);
+        }
+        for (int q = 0; q < kTilesPerUnit; ++q) {
+            mbar_init(bar(kBarSfull + q), 1);
+            mbar_init(bar(kBarPfull + q), 4);
+            mbar_init(bar(kBarOfull + q), 1);
+            mbar_init(bar(kBarOfree + q), 4);
+        }
+        mbar_init(bar(kBarFinal), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t nk = 0, nv = 0, it = 0;  // K tiles, V tiles and Q pairs issued
+            bool ok = true;
+            for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x) {
+                Work u;
+                decode(p, w, u);
+                if (!(ok = mbar_wait(bar(kBarQfree), (it & 1) ^ 1, abort_flag, p.status, kSiteQfree, tlim)))
+                    break;
+                mbar_arrive_expect_tx(bar(kBarQfull), (uint32_t)(u.nact * L::kTileBytes));
+                for (int q = 0; q < u.nact; ++q) {
+                    const int row = tile_row(u, q);
+                    for (int hf = 0; hf < D / 64; ++hf)
+                        tma_load_4d(sbase + L::kQ + q * L::kTileBytes + hf * kHalfBytes, &tm_q,
+                                    bar(kBarQfull), hf * 64, row, u.h, u.b);
+                }
+                ++it;
+                for (int j = 0; j < u.nkt; ++j) {
+                    int start, nvalid;
+                    key_tile(u, j, start, nvalid);
+                    const int st = nk % kStages;
+                    const uint32_t par = ((nk / kStages) & 1) ^ 1;
+                    if (!(ok = mbar_wait(bar(kBarKfree + st), par, abort_flag, p.status, kSiteKfree, tlim)))
+                        break;
+                    mbar_arrive_expect_tx(bar(kBarKfull + st), L::kTileBytes);
+                    for (int hf = 0; hf < D / 64; ++hf)
+                        tma_load_4d(sbase + L::kK + st * L::kTileBytes + hf * kHalfBytes, &tm_k,
+                                    bar(kBarKfull + st), hf * 64, start, u.h, u.b);
+                    ++nk;
+                    if (!(ok = mbar_wait(bar(kBarVfree + st), par, abort_flag, p.status, kSiteVfree, tlim)))
+                        break;
+                    mbar_arrive_expect_tx(bar(kBarVfull + st), L::kTileBytes);
+                    for (int hf = 0; hf < D / 64; ++hf)
+                        tma_load_4d(sbase + L::kV + st * L::kTileBytes + hf * kHalfBytes, &tm_v,
+                                    bar(kBarVfull + st), hf * 64, start, u.h, u.b);
+                    ++nv;
+                }
+            }
+            // drain: every copy this thread issued must land before the CTA exits
+            for (int s = 0; s < kStages; ++s) {
+                const uint32_t n_k = nk / kStages + ((uint32_t)s < nk % kStages ? 1u : 0u);
+                const uint32_t n_v = nv / kStages + ((uint32_t)s < nv % kStages ? 1u : 0u);
+                if (n_k > 0) drain_wait(bar(kBarKfull + s), (n_k - 1) & 1, tlim);
+                if (n_v > 0) drain_wait(bar(kBarVfull + s), (n_v - 1) & 1, tlim);
+            }
+            if (it > 0) drain_wait(bar(kBarQfull), (it - 1) & 1, tlim);
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_pv = idesc_bf16(128, D, true);
+            uint32_t kc = 0, it = 0, sq[kTilesPerUnit] = {0, 0}, uq[kTilesPerUnit] = {0, 0};
+            bool ok = true;
+            auto issue_s = [&](int q, int st, int nmma) {
+                const uint32_t idesc = idesc_bf16(128, nmma, false);
+                const uint32_t qa = sbase + L::kQ + q * L::kTileBytes;
+                const uint32_t ka = sbase + L::kK + st * L::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kHalfBytes + (ks % 4) * 32;
+                    mma_ss(tmem + L::kTmemS + q * 128, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), idesc, ks > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int q, int st, int nmma, bool acc) {
+                const uint32_t va = sbase + L::kV + st * L::kTileBytes;
+                for (int ks = 0; ks < nmma / 16; ++ks) {
+                    mma_ts(tmem + L::kTmemO + q * D, tmem + L::kTmemS + q * 128 + ks * 8,
+                           sdesc_sw128(va + ks * 2048, kHalfBytes, 1024), idesc_pv,
+                           (acc || ks > 0) ? 1u : 0u);
+                }
+            };
+            for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
+                Work u;
+                decode(p, w, u);
+                if (!(ok = mbar_wait(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullMma, tlim)))
+                    break;
+                const uint32_t kc0 = kc;
+                int start, nvalid;
+                key_tile(u, 0, start, nvalid);
+                {
+                    const int st = kc0 % kStages;
+                    if (!(ok = mbar_wait(bar(kBarKfull + st), (kc0 / kStages) & 1, abort_flag, p.status,
+                                         kSiteKfull, tlim)))
+                        break;
+                    tc_fence_after();
+                    for (int q = 0; q < u.nact; ++q) {
+                        issue_s(q, st, (nvalid + 15) & ~15);
+                        mma_commit(bar(kBarSfull + q));
+                    }
+                    mma_commit(bar(kBarKfree + st));
+                    if (u.nkt == 1) mma_commit(bar(kBarQfree));
+                }
+                for (int j = 0; j < u.nkt && ok; ++j) {
+                    const uint32_t c = kc0 + j;
+                    const int st = c % kStages;
+                    key_tile(u, j, start, nvalid);
+                    const int nmma = (nvalid + 15) & ~15;
+                    int start1 = 0, nvalid1 = 0;
+                    if (j + 1 < u.nkt) key_tile(u, j + 1, start1, nvalid1);
+                    if (!(ok = mbar_wait(bar(kBarVfull + st), (c / kStages) & 1, abort_flag, p.status,
+                                         kSiteVfull, tlim)))
+                        break;
+                    for (int q = 0; q < u.nact && ok; ++q) {
+                        if (!(ok = mbar_wait(bar(kBarPfull + q), sq[q] & 1, abort_flag, p.status,
+                                             kSitePfull, tlim)))
+                            break;
+                        if (j == 0 && !(ok = mbar_wait(bar(kBarOfree + q), (uq[q] & 1) ^ 1, abort_flag,
+                                                       p.status, kSiteOfree, tlim)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(q, st, nmma, j > 0);
+                        ++sq[q];
+                        if (q == u.nact - 1) mma_commit(bar(kBarVfree + st));
+                        if (j == u.nkt - 1) mma_commit(bar(kBarOfull + q));
+                        if (j + 1 < u.nkt) {
+                            const uint32_t c1 = c + 1;
+                            const int st1 = c1 % kStages;
+                            if (q == 0) {
+                                if (!(ok = mbar_wait(bar(kBarKfull + st1), (c1 / kStages) & 1, abort_flag,
+                                                     p.status, kSiteKfull, tlim)))
+                                    break;
+                                tc_fence_after();
+                            }
+                            issue_s(q, st1, (nvalid1 + 15) & ~15);
+                            mma_commit(bar(kBarSfull + q));
+                            if (q == u.nact - 1) {
+                                mma_commit(bar(kBarKfree + st1));
+                                if (j + 1 == u.nkt - 1) mma_commit(bar(kBarQfree));
+                            }
+                        }
+                    }
+                }
+                for (int q = 0; q < u.nact; ++q) ++uq[q];
+                kc += u.nkt;
+            }
+            // drain: all issued MMAs complete before TMEM is released
+            mma_commit(bar(kBarFinal));
+            drain_wait(bar(kBarFinal), 0, tlim);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int q = warp / 4;                  // query tile of this warpgroup
+        const int r = threadIdx.x % kTileRows;   // row within the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
+        const uint32_t tS = tmem + L::kTmemS + q * 128 + lane_off;
+        const uint32_t tO = tmem + L::kTmemO + q * D + lane_off;
+        const float sc = p.scale_log2;
+        uint32_t it = 0, sq = 0, uq = 0;
+        bool ok = true;
+        for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
+            Work u;
+            decode(p, w, u);
+            const bool act = q < u.nact;
+            const bool stat = p.mode == VDIT_MODE_FORCE_STATIC ||
+                              (p.mode == VDIT_MODE_AUTO && p.elig[u.bh] != 0);
+            ok = mbar_wait(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            // row bound ("Unchaining the Softmax"): m~ = scale*log2e*(q.c + |q| R)
+            float mt = 0.f;
+            if (act && stat) {
+                const uint8_t *qt = smem + L::kQ + q * L::kTileBytes;
+                const float *cm = p.k_mean + (size_t)u.bh * D;
+                float dot = 0.f, nn = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < D / 64; ++hf) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            qt + hf * kHalfBytes + r * 128 + ((ch ^ (r & 7)) * 16));
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = __uint_as_float(wv[e] << 16);
+                            const float x1 = __uint_as_float(wv[e] & 0xFFFF0000u);
+                            const int d = hf * 64 + ch * 8 + 2 * e;
+                            dot = fmaf(x0, cm[d], dot);
+                            dot = fmaf(x1, cm[d + 1], dot);
+                            nn = fmaf(x0, x0, nn);
+                            nn = fmaf(x1, x1, nn);
+                        }
+                    }
+                }
+                mt = sc * (dot + sqrtf(nn) * p.k_rmax[u.bh]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarQfree));
+            if (!act) continue;
+
+            float l0 = 0.f, l1 = 0.f, mrun = -INFINITY;
+            for (int j = 0; j < u.nkt; ++j) {
+                int start, nvalid;
+                key_tile(u, j, start, nvalid);
+                const int nmma = (nvalid + 15) & ~15;
+                ok = mbar_wait(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                float mrow = mt;
+                if (!stat) {
+                    // online: this tile's row max (pass 1), lazy rescale of O
+                    float mx = -INFINITY;
+                    for (int c0 = 0; c0 < nmma; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tS + c0, v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float x = __uint_as_float(v[e]) * sc;
+                            mx = (c0 + e < nvalid) ? fmaxf(mx, x) : mx;
+                        }
+                    }
+                    if (j == 0) {
+                        mrun = mx;
+                    } else {
+                        const bool need = mx > mrun + kLazyRescale;
+                        if (__any_sync(0xffffffffu, need)) {
+                            const float alpha = need ? ex2(mrun - mx) : 1.f;
+#pragma unroll
+                            for (int c0 = 0; c0 < D; c0 += 32) {
+                                uint32_t v[32];
+                                tmem_ld32(tO + c0, v);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                                tmem_st32(tO + c0, v);
+                            }
+                            l0 *= alpha;
+                            l1 *= alpha;
+                            if (need) mrun = mx;
+                        }
+                    }
+                    mrow = mrun;
+                }
+                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S
+                for (int c0 = 0; c0 < nmma; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + c0, v);
+                    uint32_t pk[16];
+                    if (c0 + 32 <= nvalid) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -mrow));
+                            const float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mrow));
+                            l0 += p0;
+                            l1 += p1;
+                            pk[e] = pack_bf16(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int col = c0 + 2 * e;
+                            const float p0 = col < nvalid
+                                                 ? ex2(fmaf(__uint_as_float(v[2 * e]), sc, -mrow))
+                                                 : 0.f;
+                            const float p1 = col + 1 < nvalid
+                                                 ? ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mrow))
+                                                 : 0.f;
+                            l0 += p0;
+                            l1 += p1;
+                            pk[e] = pack_bf16(p0, p1);
+                        }
+                    }
+                    tmem_st16(tS + c0 / 2, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarPfull + q));
+                ++sq;
+                if (!stat) mt = mrun;
+            }
+            if (!ok) break;
+            ok = mbar_wait(bar(kBarOfull + q), uq & 1, abort_flag, p.status, kSiteOfull, tlim);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            // epilogue: O / l for the rows this tile owns, and LSE
+            const float l = l0 + l1;
+            const float inv = 1.0f / l;
+            const int t = kTilesPerUnit * u.pair + q;
+            const int row = tile_row(u, q) + r;
+            const int own_lo = u.row0 + t * kTileRows;
+            const int own_hi = u.row0 + min((t + 1) * kTileRows, u.rows);
+            const bool owned = row >= own_lo && row < own_hi;
+            const long long obase = (long long)u.b * p.os0 + (long long)u.h * p.os1 + (long long)row * p.os2;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tO + c0, v);
+                if (owned) {
+                    if (p.o_f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + obase + c0);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(v[4 * e]) * inv,
+                                                 __uint_as_float(v[4 * e + 1]) * inv,
+                                                 __uint_as_float(v[4 * e + 2]) * inv,
+                                                 __uint_as_float(v[4 * e + 3]) * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + obase + c0);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 o4;
+                            o4.x = pack_bf16(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv);
+                            o4.y = pack_bf16(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv);
+                            o4.z = pack_bf16(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv);
+                            o4.w = pack_bf16(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv);
+                            dst[e] = o4;
+                        }
+                    }
+                }
+            }
+            if (owned && p.lse)
+                p.lse[((long long)u.bh * p.N) + row] = (mt + log2f(l)) * 0.69314718055994531f;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarOfree + q));
+            ++uq;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &qres) == cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [B, H, N, D] bf16 tensor -> 4-D tensor map with a 64 x 128 x 1 x 1 box, 128-byte swizzle.
+bool encode_bhnd(CUtensorMap *m, const void *base, int B, int H, int N, int D, const int64_t st[3]) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Both head dims request the D = 128 shared-memory size: one CTA (and so one
+// TMEM owner) per SM.
+constexpr int kSmemRequest = Layout<128>::kAlloc;
+
+template <int D>
+cudaError_t prepare_kernel(int device) {
+    static std::mutex mu;
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemRequest);
+    if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
+    return e;
+}
+
+int sm_count(int device) {
+    static std::mutex mu;
+    static int cache[64] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (device < 0 || device >= 64) return 0;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess)
+            cache[device] = n;
+    }
+    return cache[device];
+}
+
+}  // namespace
+}  // namespace vdit
+
+using namespace vdit;
+
+extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k,
+                                     const void *v, void *o, int32_t o_dtype, float *lse,
+                                     int32_t B, int32_t H, int32_t D, const int64_t q_strides[3],
+                                     const int64_t k_strides[3], const int64_t v_strides[3],
+                                     const int64_t o_strides[3], float scale, const float *k_mean,
+                                     const float *k_rmax, const uint8_t *eligible, int32_t mode,
+                                     void *stream) {
+    clear_error();
+    if (!plan) { set_error("vdit_attn_fwd: plan is NULL"); return VDIT_ERR_INVALID; }
+    if (!q || !k || !v || !o || !q_strides || !k_strides || !v_strides || !o_strides) {
+        set_error("vdit_attn_fwd: NULL tensor or stride argument");
+        return VDIT_ERR_INVALID;
+    }
+    if (B < 1 || H < 1) { set_error("vdit_attn_fwd: B=%d H=%d must be >= 1", B, H); return VDIT_ERR_INVALID; }
+    if (D != 64 && D != 128) {
+        set_error("vdit_attn_fwd: head dim D=%d not supported (64 or 128)", D);
+        return VDIT_ERR_UNSUPPORTED;
+    }
+    if (o_dtype != VDIT_O_BF16 && o_dtype != VDIT_O_F32) {
+        set_error("vdit_attn_fwd: o_dtype=%d invalid", o_dtype);
+        return VDIT_ERR_INVALID;
+    }
+    if (mode < VDIT_MODE_AUTO || mode > VDIT_MODE_FORCE_STATIC) {
+        set_error("vdit_attn_fwd: mode=%d invalid", mode);
+        return VDIT_ERR_INVALID;
+    }
+    if (mode != VDIT_MODE_FORCE_ONLINE && (!k_mean || !k_rmax)) {
+        set_error("vdit_attn_fwd: k_mean and k_rmax are required unless mode is FORCE_ONLINE");
+        return VDIT_ERR_INVALID;
+    }
+    if (mode == VDIT_MODE_AUTO && !eligible) {
+        set_error("vdit_attn_fwd: eligible is required in AUTO mode");
+        return VDIT_ERR_INVALID;
+    }
+    if (!(scale > 0.f)) { set_error("vdit_attn_fwd: scale must be > 0"); return VDIT_ERR_INVALID; }
+    const int64_t *sts[3] = {q_strides, k_strides, v_strides};
+    for (int t = 0; t < 3; ++t)
+        for (int i = 0; i < 3; ++i)
+            if (sts[t][i] <= 0 || sts[t][i] % 8 != 0 || sts[t][i] >= (1ll << 38)) {
+                set_error("vdit_attn_fwd: q/k/v strides must be positive multiples of 8 elements");
+                return VDIT_ERR_INVALID;
+            }
+    const int oal = o_dtype == VDIT_O_F32 ? 4 : 8;
+    for (int i = 0; i < 3; ++i)
+        if (o_strides[i] <= 0 || o_strides[i] % oal != 0) {
+            set_error("vdit_attn_fwd: o strides must be positive multiples of 16 bytes");
+            return VDIT_ERR_INVALID;
+        }
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) {
+        set_error("vdit_attn_fwd: q, k, v, o must be 16-byte aligned");
+        return VDIT_ERR_INVALID;
+    }
+    int dev = -1;
+    VDIT_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != plan->device) {
+        set_error("vdit_attn_fwd: plan was built on device %d, current device is %d", plan->device, dev);
+        return VDIT_ERR_INVALID;
+    }
+    const int N = (int)plan->N;
+    CUtensorMap tq, tk, tv;
+    if (!encode_bhnd(&tq, q, B, H, N, D, q_strides) || !encode_bhnd(&tk, k, B, H, N, D, k_strides) ||
+        !encode_bhnd(&tv, v, B, H, N, D, v_strides)) {
+        set_error("vdit_attn_fwd: cuTensorMapEncodeTiled failed (alignment/strides or driver entry point)");
+        return VDIT_ERR_INVALID;
+    }
+    Params prm;
+    prm.segments = plan->d_segments;
+    prm.units = plan->d_units;
+    prm.class_off = plan->d_class_off;
+    prm.n_classes = plan->h.n_classes;
+    prm.B = B; prm.H = H; prm.N = N;
+    prm.total_work = (long long)B * H * plan->h.n_units;
+    prm.o = o;
+    prm.os0 = o_strides[0]; prm.os1 = o_strides[1]; prm.os2 = o_strides[2];
+    prm.o_f32 = o_dtype == VDIT_O_F32;
+    prm.lse = lse;
+    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.k_mean = k_mean; prm.k_rmax = k_rmax; prm.elig = eligible;
+    prm.mode = mode;
+    prm.status = plan->d_status;
+    prm.timeout_ns = kDefaultTimeoutNs;
+    const int nsm = sm_count(dev);
+    if (nsm <= 0) { set_error("vdit_attn_fwd: cannot query SM count"); return VDIT_ERR_CUDA; }
+    const long long grid = prm.total_work < nsm ? prm.total_work : nsm;
+    if (grid <= 0) return VDIT_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (D == 128) {
+        VDIT_CUDA_TRY(prepare_kernel<128>(dev));
+        attn_fwd_kernel<128><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    } else {
+        VDIT_CUDA_TRY(prepare_kernel<64>(dev));
+        attn_fwd_kernel<64><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    }
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
+}

@@ -1,0 +1,68 @@
+// Host-side internals shared by the libvdit translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "vdit.h"
+
+namespace vdit {
+
+// Thread-local error text behind vdit_last_error().
+void set_error(const char *fmt, ...);
+void clear_error();
+
+// Formats a CUDA error into the thread-local message and returns VDIT_ERR_CUDA.
+vdit_status cuda_fail(cudaError_t e, const char *what);
+
+#define VDIT_CUDA_TRY(expr)                                      \
+    do {                                                         \
+        cudaError_t e__ = (expr);                                \
+        if (e__ != cudaSuccess) return ::vdit::cuda_fail(e__, #expr); \
+    } while (0)
+
+// Query-tile geometry shared by the plan and the attention kernel.
+constexpr int kTileRows = 128;   // rows of one query tile (tcgen05 M)
+constexpr int kTilesPerUnit = 2; // query tiles that share one K/V stream
+constexpr int kSegInts = 8;      // ints per segment record
+constexpr int kMaxFrames = 4096; // frames a plan may hold
+constexpr int kMaxClasses = 64;  // distinct unit costs a plan may hold
+
+// Header the schedule kernel writes (device), read back once by the host.
+struct PlanHeader {
+    long long nnz;
+    long long live_pairs;
+    int n_segments;
+    int n_units;
+    int n_classes;
+    int error; // non-zero: the kernel found an inconsistent request
+};
+
+}  // namespace vdit
+
+struct vdit_plan {
+    int F, T, W, ref, bs, dense;
+    long long N;
+    int n_qblocks;
+    vdit::PlanHeader h;  // host copy of the header
+    int device;
+    // device buffers (owned)
+    vdit::PlanHeader *d_header = nullptr;
+    int32_t *d_row_ptr = nullptr;
+    int32_t *d_col_idx = nullptr;
+    int32_t *d_frame_runs = nullptr;
+    int32_t *d_segments = nullptr;
+    int32_t *d_units = nullptr;
+    int32_t *d_class_off = nullptr;
+    int32_t *d_status = nullptr;
+    int units_cap = 0;
+};
+
+namespace vdit {
+// Launches the two schedule kernels for `p` on `stream` (buffers must exist;
+// col_idx may be null when only the meta kernel should run).
+cudaError_t launch_plan_kernels(const vdit_plan *p, cudaStream_t stream, bool csr);
+}  // namespace vdit

@@ -1,0 +1,360 @@
+// Block schedule of the frame-window + reference-frame mask.
+//
+// "HeyGen x Google Cloud: Bringing Avatar IV to TPUs", "Deleting the Mask"
+// (Fig. 3): a query in frame f sees the keys of frames g with |f - g| <= W
+// (clipped to the sequence) plus the reference frame. With a block size that
+// is a multiple of 16 and divides the frame's token span, each block is either
+// entirely live or entirely dead, and the reference frame's blocks are simply
+// more live blocks of the same pass.
+//
+// Two kernels build the plan on the device:
+//   plan_meta_kernel  per-frame key runs (at most two maximal runs of live key
+//                     tokens: the window and, when outside it, the reference
+//                     frame), segments of consecutive frames sharing one run
+//                     list, the attention kernel's work units ordered longest
+//                     first, and the header counts (nnz, live pairs).
+//   plan_csr_kernel   the CSR of live (query block, key block) pairs.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <new>
+
+#include "vdit_internal.h"
+
+namespace vdit {
+namespace {
+
+struct PlanArgs {
+    int F, T, W, ref, bs, dense;
+    long long N;
+    int nqb;
+    int units_cap;
+};
+
+// Window [wlo, whi] of frame f and whether the reference frame adds a run.
+__device__ __forceinline__ void frame_window(const PlanArgs &a, int f, int &wlo, int &whi) {
+    wlo = f - a.W < 0 ? 0 : f - a.W;
+    whi = f + a.W > a.F - 1 ? a.F - 1 : f + a.W;
+}
+
+// Live key frames of frame f, as at most two maximal token runs [lo, hi).
+__device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_frames) {
+    int wlo, whi;
+    frame_window(a, f, wlo, whi);
+    long long T = a.T;
+    live_frames = whi - wlo + 1;
+    int lo0 = (int)(wlo * T), hi0 = (int)((whi + 1) * T), lo1 = 0, hi1 = 0;
+    const int g = a.ref;
+    if (g >= 0 && (g < wlo || g > whi)) {
+        live_frames += 1;
+        if (g == wlo - 1) {
+            lo0 = (int)(g * T);                       // adjacent below: merge
+        } else if (g == whi + 1) {
+            hi0 = (int)((g + 1) * T);                 // adjacent above: merge
+        } else if (g < wlo) {
+            lo1 = lo0; hi1 = hi0;                     // reference run first
+            lo0 = (int)(g * T); hi0 = (int)((g + 1) * T);
+        } else {
+            lo1 = (int)(g * T); hi1 = (int)((g + 1) * T);
+        }
+    }
+    r[0] = lo0; r[1] = hi0; r[2] = lo1; r[3] = hi1;
+}
+
+__global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_runs,
+                                 int32_t *segments, int32_t *units, int32_t *class_off) {
+    __shared__ int s_cnt[kMaxFrames];
+    __shared__ int s_order[kMaxFrames];
+    for (int f = threadIdx.x; f < a.F; f += blockDim.x) {
+        int r[4], live;
+        frame_runs_of(a, f, r, live);
+        frame_runs[4 * f + 0] = r[0];
+        frame_runs[4 * f + 1] = r[1];
+        frame_runs[4 * f + 2] = r[2];
+        frame_runs[4 * f + 3] = r[3];
+        s_cnt[f] = live;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+
+    PlanHeader h{};
+    // counts ------------------------------------------------------------
+    long long fp = 0;
+    for (int f = 0; f < a.F; ++f) fp += s_cnt[f];
+    h.live_pairs = fp * (long long)a.T * a.T;
+    if (a.dense) {
+        h.nnz = (long long)a.nqb * a.nqb;
+    } else {
+        long long per = a.T / a.bs;
+        h.nnz = fp * per * per;
+    }
+    // segments: consecutive frames with identical run lists --------------
+    int nseg = 0;
+    for (int f = 0; f < a.F; ++f) {
+        const int32_t *r = frame_runs + 4 * f;
+        bool same = false;
+        if (f > 0) {
+            const int32_t *p = frame_runs + 4 * (f - 1);
+            same = p[0] == r[0] && p[1] == r[1] && p[2] == r[2] && p[3] == r[3];
+        }
+        if (same) {
+            int32_t *s = segments + kSegInts * (nseg - 1);
+            s[1] += a.T;
+        } else {
+            int32_t *s = segments + kSegInts * nseg;
+            s[0] = (int)((long long)f * a.T);
+            s[1] = a.T;
+            s[2] = r[0]; s[3] = r[1]; s[4] = r[2]; s[5] = r[3];
+            s[7] = (r[1] - r[0]) + (r[3] - r[2]);
+            ++nseg;
+        }
+    }
+    for (int s = 0; s < nseg; ++s) {
+        int32_t *g = segments + kSegInts * s;
+        g[6] = (g[1] + kTileRows - 1) / kTileRows;
+        s_order[s] = s;
+    }
+    // longest first (stable insertion sort on key count) ------------------
+    for (int i = 1; i < nseg; ++i) {
+        int v = s_order[i], key = segments[kSegInts * v + 7], j = i - 1;
+        while (j >= 0 && segments[kSegInts * s_order[j] + 7] < key) {
+            s_order[j + 1] = s_order[j];
+            --j;
+        }
+        s_order[j + 1] = v;
+    }
+    int nu = 0, ncls = 0, prev_key = -1;
+    for (int i = 0; i < nseg; ++i) {
+        int s = s_order[i];
+        const int32_t *g = segments + kSegInts * s;
+        if (g[7] != prev_key) {
+            if (ncls >= kMaxClasses) { h.error = 2; break; }
+            class_off[ncls++] = nu;
+            prev_key = g[7];
+        }
+        int npairs = (g[6] + kTilesPerUnit - 1) / kTilesPerUnit;
+        for (int p = 0; p < npairs; ++p) {
+            if (nu >= a.units_cap) { h.error = 3; break; }
+            units[nu++] = (s << 16) | p;
+        }
+    }
+    class_off[ncls] = nu;
+    h.n_segments = nseg;
+    h.n_units = nu;
+    h.n_classes = ncls;
+    *hdr = h;
+}
+
+__global__ void plan_csr_kernel(PlanArgs a, const int32_t *frame_runs, int32_t *row_ptr,
+                                int32_t *col_idx) {
+    const int qb = blockIdx.x * blockDim.x + threadIdx.x;
+    if (qb >= a.nqb) return;
+    long long start;
+    if (a.dense) {
+        start = (long long)qb * a.nqb;
+        for (int kb = 0; kb < a.nqb; ++kb) col_idx[start + kb] = kb;
+    } else {
+        const int per = a.T / a.bs;
+        const int f = qb / per;
+        long long before = 0;
+        for (int g = 0; g < f; ++g) {
+            const int32_t *r = frame_runs + 4 * g;
+            before += (long long)((r[1] - r[0]) + (r[3] - r[2])) / a.bs;
+        }
+        const int32_t *r = frame_runs + 4 * f;
+        const int row_len = ((r[1] - r[0]) + (r[3] - r[2])) / a.bs;
+        start = before * per + (long long)(qb - f * per) * row_len;
+        long long k = start;
+        for (int run = 0; run < 2; ++run) {
+            for (int kb = r[2 * run] / a.bs; kb < r[2 * run + 1] / a.bs; ++kb) col_idx[k++] = kb;
+        }
+    }
+    row_ptr[qb] = (int32_t)start;
+    if (qb == a.nqb - 1) {
+        long long len = a.dense ? a.nqb
+                                : ((frame_runs[4 * (a.F - 1) + 1] - frame_runs[4 * (a.F - 1)]) +
+                                   (frame_runs[4 * (a.F - 1) + 3] - frame_runs[4 * (a.F - 1) + 2])) /
+                                      a.bs;
+        row_ptr[a.nqb] = (int32_t)(start + len);
+    }
+}
+
+PlanArgs args_of(const vdit_plan *p) {
+    PlanArgs a;
+    a.F = p->F; a.T = p->T; a.W = p->W; a.ref = p->ref; a.bs = p->bs; a.dense = p->dense;
+    a.N = p->N; a.nqb = p->n_qblocks; a.units_cap = p->units_cap;
+    return a;
+}
+
+void free_plan_buffers(vdit_plan *p) {
+    cudaFree(p->d_header);
+    cudaFree(p->d_row_ptr);
+    cudaFree(p->d_col_idx);
+    cudaFree(p->d_frame_runs);
+    cudaFree(p->d_segments);
+    cudaFree(p->d_units);
+    cudaFree(p->d_class_off);
+    cudaFree(p->d_status);
+}
+
+}  // namespace
+
+cudaError_t launch_plan_kernels(const vdit_plan *p, cudaStream_t stream, bool csr) {
+    PlanArgs a = args_of(p);
+    plan_meta_kernel<<<1, 256, 0, stream>>>(a, p->d_header, p->d_frame_runs, p->d_segments,
+                                             p->d_units, p->d_class_off);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !csr) return e;
+    plan_csr_kernel<<<(a.nqb + 255) / 256, 256, 0, stream>>>(a, p->d_frame_runs, p->d_row_ptr,
+                                                             p->d_col_idx);
+    return cudaGetLastError();
+}
+
+}  // namespace vdit
+
+using namespace vdit;
+
+extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs,
+                                      void *stream, vdit_plan **out) {
+    clear_error();
+    if (!out) { set_error("vdit_attn_plan: out is NULL"); return VDIT_ERR_INVALID; }
+    *out = nullptr;
+    if (F < 1 || F > kMaxFrames) {
+        set_error("vdit_attn_plan: num_frames=%d outside [1, %d]", F, kMaxFrames);
+        return VDIT_ERR_INVALID;
+    }
+    if (T < 1) { set_error("vdit_attn_plan: tokens_per_frame=%d < 1", T); return VDIT_ERR_INVALID; }
+    if ((long long)F * T >= (1ll << 31)) {
+        set_error("vdit_attn_plan: N = F*T = %lld does not fit int32", (long long)F * T);
+        return VDIT_ERR_INVALID;
+    }
+    if (W < 0) { set_error("vdit_attn_plan: window_radius=%d < 0", W); return VDIT_ERR_INVALID; }
+    if (ref < -1 || ref >= F) {
+        set_error("vdit_attn_plan: ref_frame=%d outside [-1, %d]", ref, F - 1);
+        return VDIT_ERR_INVALID;
+    }
+    if (bs < 16 || bs % 16 != 0) {
+        set_error("vdit_attn_plan: block_size=%d is not a positive multiple of 16", bs);
+        return VDIT_ERR_INVALID;
+    }
+    const int dense = W >= F - 1 ? 1 : 0;
+    if (!dense && T % bs != 0) {
+        set_error("vdit_attn_plan: block_size=%d does not divide tokens_per_frame=%d "
+                  "(blocks would straddle frame boundaries)", bs, T);
+        return VDIT_ERR_INVALID;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    vdit_plan *p = new (std::nothrow) vdit_plan();
+    if (!p) { set_error("vdit_attn_plan: host allocation failed"); return VDIT_ERR_NOMEM; }
+    p->F = F; p->T = T; p->W = W; p->ref = ref; p->bs = bs; p->dense = dense;
+    p->N = (long long)F * T;
+    p->n_qblocks = (int)((p->N + bs - 1) / bs);
+    p->units_cap = (int)(p->N / (kTileRows * kTilesPerUnit)) + 2 * F + 2;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
+    e = cudaMalloc(&p->d_header, sizeof(PlanHeader));
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_frame_runs, sizeof(int32_t) * 4 * F);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_segments, sizeof(int32_t) * kSegInts * F);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_units, sizeof(int32_t) * p->units_cap);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_class_off, sizeof(int32_t) * (kMaxClasses + 1));
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) {
+        free_plan_buffers(p);
+        delete p;
+        set_error("vdit_attn_plan: device allocation failed (%s)", cudaGetErrorString(e));
+        return VDIT_ERR_NOMEM;
+    }
+    e = launch_plan_kernels(p, s, false);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&p->h, p->d_header, sizeof(PlanHeader),
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        free_plan_buffers(p);
+        delete p;
+        return cuda_fail(e, "vdit_attn_plan: schedule kernel");
+    }
+    if (p->h.error != 0 || p->h.nnz >= (1ll << 31)) {
+        set_error("vdit_attn_plan: schedule too large (error %d, nnz %lld)", p->h.error, p->h.nnz);
+        free_plan_buffers(p);
+        delete p;
+        return VDIT_ERR_INVALID;
+    }
+    e = cudaMalloc(&p->d_row_ptr, sizeof(int32_t) * (p->n_qblocks + 1));
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_col_idx, sizeof(int32_t) * (p->h.nnz > 0 ? p->h.nnz : 1));
+    if (e != cudaSuccess) {
+        free_plan_buffers(p);
+        delete p;
+        set_error("vdit_attn_plan: device allocation failed (%s)", cudaGetErrorString(e));
+        return VDIT_ERR_NOMEM;
+    }
+    e = launch_plan_kernels(p, s, true);
+    if (e != cudaSuccess) {
+        free_plan_buffers(p);
+        delete p;
+        return cuda_fail(e, "vdit_attn_plan: schedule kernels");
+    }
+    *out = p;
+    return VDIT_OK;
+}
+
+extern "C" vdit_status vdit_plan_rebuild(vdit_plan *p, void *stream) {
+    clear_error();
+    if (!p) { set_error("vdit_plan_rebuild: plan is NULL"); return VDIT_ERR_INVALID; }
+    cudaError_t e = launch_plan_kernels(p, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return cuda_fail(e, "vdit_plan_rebuild");
+    return VDIT_OK;
+}
+
+extern "C" vdit_status vdit_plan_get_info(const vdit_plan *p, vdit_plan_info *info) {
+    clear_error();
+    if (!p || !info) { set_error("vdit_plan_get_info: NULL argument"); return VDIT_ERR_INVALID; }
+    info->num_frames = p->F;
+    info->tokens_per_frame = p->T;
+    info->window_radius = p->W;
+    info->ref_frame = p->ref;
+    info->block_size = p->bs;
+    info->dense = p->dense;
+    info->num_tokens = p->N;
+    info->n_qblocks = p->n_qblocks;
+    info->nnz = p->h.nnz;
+    info->live_pairs = p->h.live_pairs;
+    info->n_segments = p->h.n_segments;
+    info->n_units = p->h.n_units;
+    info->n_classes = p->h.n_classes;
+    info->d_row_ptr = p->d_row_ptr;
+    info->d_col_idx = p->d_col_idx;
+    info->d_frame_runs = p->d_frame_runs;
+    info->d_segments = p->d_segments;
+    info->d_units = p->d_units;
+    info->d_class_off = p->d_class_off;
+    return VDIT_OK;
+}
+
+extern "C" vdit_status vdit_plan_status(vdit_plan *p, void *stream, int32_t *code) {
+    clear_error();
+    if (!p) { set_error("vdit_plan_status: plan is NULL"); return VDIT_ERR_INVALID; }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    VDIT_CUDA_TRY(cudaMemcpyAsync(&word, p->d_status, sizeof word, cudaMemcpyDeviceToHost, s));
+    VDIT_CUDA_TRY(cudaStreamSynchronize(s));
+    if (code) *code = word;
+    if (word != 0) {
+        VDIT_CUDA_TRY(cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s));
+        VDIT_CUDA_TRY(cudaStreamSynchronize(s));
+        set_error("a kernel's bounded wait expired (site code %d)", word);
+        return VDIT_ERR_TIMEOUT;
+    }
+    return VDIT_OK;
+}
+
+extern "C" void vdit_plan_destroy(vdit_plan *p) {
+    if (!p) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    free_plan_buffers(p);
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    delete p;
+}

@@ -1,0 +1,247 @@
+// Per-head key statistics and static-max eligibility.
+//
+// "HeyGen x Google Cloud: Bringing Avatar IV to TPUs", "Unchaining the
+// Softmax": a tiny array of precomputed norms lets every query row derive an
+// upper bound on its logits as it starts; centring the keys on their mean
+// tightens that bound without changing the softmax; heads whose bound is too
+// loose fall back to online softmax. This file computes, per (b, h):
+//   c    = (1/N) sum_j k_j          R  = max_j |k_j - c|
+//   Qm   = max_i |q_i|              G  = 2 * scale * Qm * R,  eligible = G <= tau
+// HBM-bound: K is read twice (the second read mostly from L2), Q once.
+// Three launches, every reduction in a fixed order (bitwise reproducible):
+//   stats_pass1    per chunk of rows: column sums of K, max |q|^2
+//   stats_pass2    c from the chunk sums; per chunk: max |k - c|^2
+//   stats_finalize R, Qm, G, eligibility
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "vdit_internal.h"
+
+namespace vdit {
+namespace {
+
+constexpr int kRowsPerChunk = 1024;
+constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
+
+struct StatsArgs {
+    const __nv_bfloat16 *q, *k;
+    long long qs0, qs1, qs2, ks0, ks1, ks2;
+    int B, H, N, nchunk;
+    float scale, tau;
+    float *ws_colsum, *ws_qn2, *ws_rn2;
+    float *k_mean, *k_rmax, *q_nmax, *gap;
+    uint8_t *elig;
+};
+
+template <int EPT>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *row, int lane, float (&x)[EPT]) {
+    if constexpr (EPT == 4) {
+        uint2 u = *reinterpret_cast<const uint2 *>(row + lane * 4);
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u.x);
+        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u.y);
+        x[0] = __low2float(a); x[1] = __high2float(a);
+        x[2] = __low2float(b); x[3] = __high2float(b);
+    } else {
+        uint32_t u = *reinterpret_cast<const uint32_t *>(row + lane * 2);
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u);
+        x[0] = __low2float(a); x[1] = __high2float(a);
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
+    constexpr int EPT = D / 32;
+    __shared__ float s_col[kStatsWarps][D];
+    __shared__ float s_q[kStatsWarps];
+    const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1;
+    const __nv_bfloat16 *qb = a.q + b * a.qs0 + h * a.qs1;
+    const int r0 = chunk * kRowsPerChunk;
+    const int r1 = min(a.N, r0 + kRowsPerChunk);
+    float acc[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+    float qm2 = 0.f;
+    for (int r = r0 + warp; r < r1; r += kStatsWarps) {
+        float x[EPT];
+        load_row<EPT>(kb + r * a.ks2, lane, x);
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) acc[e] += x[e];
+        load_row<EPT>(qb + r * a.qs2, lane, x);
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) s = fmaf(x[e], x[e], s);
+        qm2 = fmaxf(qm2, warp_sum(s));
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) s_col[warp][lane * EPT + e] = acc[e];
+    if (lane == 0) s_q[warp] = qm2;
+    __syncthreads();
+    const size_t slot = (size_t)bh * a.nchunk + chunk;
+    for (int d = threadIdx.x; d < D; d += kStatsThreads) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStatsWarps; ++w) s += s_col[w][d];
+        a.ws_colsum[slot * D + d] = s;
+    }
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kStatsWarps; ++w) m = fmaxf(m, s_q[w]);
+        a.ws_qn2[slot] = m;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
+    constexpr int EPT = D / 32;
+    __shared__ float s_c[D];
+    __shared__ float s_r[kStatsWarps];
+    const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int d = threadIdx.x; d < D; d += kStatsThreads) {
+        float s = 0.f;
+        for (int c = 0; c < a.nchunk; ++c) s += a.ws_colsum[((size_t)bh * a.nchunk + c) * D + d];
+        const float mean = s / (float)a.N;
+        s_c[d] = mean;
+        if (chunk == 0) a.k_mean[(size_t)bh * D + d] = mean;
+    }
+    __syncthreads();
+    float cm[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) cm[e] = s_c[lane * EPT + e];
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1;
+    const int r0 = chunk * kRowsPerChunk;
+    const int r1 = min(a.N, r0 + kRowsPerChunk);
+    float rm2 = 0.f;
+    for (int r = r0 + warp; r < r1; r += kStatsWarps) {
+        float x[EPT];
+        load_row<EPT>(kb + r * a.ks2, lane, x);
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            const float t = x[e] - cm[e];
+            s = fmaf(t, t, s);
+        }
+        rm2 = fmaxf(rm2, warp_sum(s));
+    }
+    if (lane == 0) s_r[warp] = rm2;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kStatsWarps; ++w) m = fmaxf(m, s_r[w]);
+        a.ws_rn2[(size_t)bh * a.nchunk + chunk] = m;
+    }
+}
+
+__global__ void stats_finalize(StatsArgs a) {
+    const int bh = blockIdx.x, lane = threadIdx.x;
+    float r2 = 0.f, q2 = 0.f;
+    for (int c = lane; c < a.nchunk; c += 32) {
+        r2 = fmaxf(r2, a.ws_rn2[(size_t)bh * a.nchunk + c]);
+        q2 = fmaxf(q2, a.ws_qn2[(size_t)bh * a.nchunk + c]);
+    }
+    r2 = warp_max(r2);
+    q2 = warp_max(q2);
+    if (lane == 0) {
+        const float R = sqrtf(r2), Qm = sqrtf(q2);
+        const float G = 2.0f * a.scale * Qm * R;
+        a.k_rmax[bh] = R;
+        a.q_nmax[bh] = Qm;
+        a.gap[bh] = G;
+        a.elig[bh] = (G <= a.tau) ? 1 : 0;
+    }
+}
+
+int nchunks(int N) { return (N + kRowsPerChunk - 1) / kRowsPerChunk; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace vdit
+
+using namespace vdit;
+
+extern "C" size_t vdit_key_stats_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D) {
+    if (B < 1 || H < 1 || N < 1 || D < 1) return 0;
+    const size_t slots = (size_t)B * H * nchunks(N);
+    return slots * (size_t)(D + 2) * sizeof(float);
+}
+
+extern "C" vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, int32_t H,
+                                      int32_t N, int32_t D, const int64_t q_strides[3],
+                                      const int64_t k_strides[3], float scale, float tau,
+                                      float *k_mean, float *k_rmax, float *q_nmax,
+                                      float *gap_bound, uint8_t *eligible, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+    clear_error();
+    if (!q || !k || !q_strides || !k_strides || !k_mean || !k_rmax || !q_nmax || !gap_bound ||
+        !eligible || !workspace) {
+        set_error("vdit_key_stats: NULL pointer argument");
+        return VDIT_ERR_INVALID;
+    }
+    if (B < 1 || H < 1 || N < 1) {
+        set_error("vdit_key_stats: B=%d H=%d N=%d must be >= 1", B, H, N);
+        return VDIT_ERR_INVALID;
+    }
+    if (D != 64 && D != 128) {
+        set_error("vdit_key_stats: head dim D=%d not supported (64 or 128)", D);
+        return VDIT_ERR_UNSUPPORTED;
+    }
+    for (int i = 0; i < 3; ++i) {
+        if (q_strides[i] <= 0 || k_strides[i] <= 0 || q_strides[i] % 8 || k_strides[i] % 8) {
+            set_error("vdit_key_stats: strides must be positive multiples of 8 elements");
+            return VDIT_ERR_INVALID;
+        }
+    }
+    if (!aligned16(q) || !aligned16(k)) {
+        set_error("vdit_key_stats: q and k must be 16-byte aligned");
+        return VDIT_ERR_INVALID;
+    }
+    const size_t need = vdit_key_stats_workspace_size(B, H, N, D);
+    if (workspace_bytes < need) {
+        set_error("vdit_key_stats: workspace of %zu bytes < %zu needed", workspace_bytes, need);
+        return VDIT_ERR_INVALID;
+    }
+    if (!(scale > 0.f) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats: scale must be > 0 and tau >= 0");
+        return VDIT_ERR_INVALID;
+    }
+    StatsArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.qs0 = q_strides[0]; a.qs1 = q_strides[1]; a.qs2 = q_strides[2];
+    a.ks0 = k_strides[0]; a.ks1 = k_strides[1]; a.ks2 = k_strides[2];
+    a.B = B; a.H = H; a.N = N; a.nchunk = nchunks(N);
+    a.scale = scale; a.tau = tau;
+    const size_t slots = (size_t)B * H * a.nchunk;
+    a.ws_colsum = static_cast<float *>(workspace);
+    a.ws_qn2 = a.ws_colsum + slots * D;
+    a.ws_rn2 = a.ws_qn2 + slots;
+    a.k_mean = k_mean; a.k_rmax = k_rmax; a.q_nmax = q_nmax; a.gap = gap_bound;
+    a.elig = eligible;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dim3 grid(a.nchunk, B * H);
+    if (D == 128) {
+        stats_pass1<128><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_pass2<128><<<grid, kStatsThreads, 0, s>>>(a);
+    } else {
+        stats_pass1<64><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
+    }
+    stats_finalize<<<B * H, 32, 0, s>>>(a);
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
+}

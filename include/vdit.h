@@ -1,0 +1,168 @@
+/*
+ * vdit.h -- C ABI of libvdit: frame-window + reference-frame block-sparse
+ * self-attention for video diffusion transformers, hand-written for sm_103a.
+ *
+ * The operation is the super-resolution stage's sparse attention described in
+ * "HeyGen x Google Cloud: Bringing Avatar IV to TPUs":
+ *   - "Deleting the Mask" (Fig. 3): every query in frame f attends to the keys
+ *     of frames g with |f - g| <= W, plus one global reference frame. Blocks
+ *     whose size is a multiple of 16 and divides the frame's token span are
+ *     entirely live or entirely dead, so one pass needs no mask predicate, no
+ *     padding and no second pass for the reference frame.
+ *   - "Unchaining the Softmax" (Fig. 4): the running max of online softmax is
+ *     replaced by a precomputed per-row upper bound on the logits,
+ *     scale * (q . c + |q| * max_j |k_j - c|), with c the per-head key mean;
+ *     heads whose bound is too loose fall back to online softmax in the same
+ *     kernel.
+ *   - "Proving the Pixels Didn't Change": the final P.V product runs in bf16.
+ *
+ * Conventions shared by every call:
+ *   - Tensors Q, K, V, O are [B, H, N, D] with the last dimension contiguous.
+ *     Strides are given in ELEMENTS for (b, h, n), as int64_t[3]. Base
+ *     addresses must be 16-byte aligned and the three strides multiples of
+ *     16 bytes (TMA requirement). N = num_frames * tokens_per_frame, tokens
+ *     frame-major. D is 64 or 128.
+ *   - Every tensor argument is caller-owned DEVICE memory; the library never
+ *     frees it. A plan owns only its own device buffers.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Every call is asynchronous on that stream, except vdit_attn_plan and
+ *     vdit_plan_status, which synchronise it once.
+ *   - Arguments are checked on the host before any launch. On error the call
+ *     launches nothing, returns a non-zero vdit_status and sets a thread-local
+ *     message readable through vdit_last_error().
+ */
+#ifndef VDIT_H
+#define VDIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VDIT_API __attribute__((visibility("default")))
+#else
+#define VDIT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VDIT_OK = 0,
+    VDIT_ERR_INVALID = 1,     /* bad argument: shape, stride, alignment, null pointer */
+    VDIT_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D not in {64,128}) */
+    VDIT_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    VDIT_ERR_NOMEM = 4,       /* device allocation for a plan failed */
+    VDIT_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (see vdit_plan_status) */
+} vdit_status;
+
+enum { VDIT_O_BF16 = 0, VDIT_O_F32 = 1 };
+enum { VDIT_MODE_AUTO = 0, VDIT_MODE_FORCE_ONLINE = 1, VDIT_MODE_FORCE_STATIC = 2 };
+
+typedef struct vdit_plan vdit_plan; /* opaque, owned by the library */
+
+/* Read-only view of a plan. All d_* pointers are device memory owned by the
+ * plan and valid until vdit_plan_destroy. Counts are per (b, h) head. */
+typedef struct {
+    int32_t num_frames, tokens_per_frame, window_radius, ref_frame, block_size;
+    int32_t dense;          /* 1 when every query sees every key (W >= F-1) */
+    int64_t num_tokens;     /* N = F * T */
+    int32_t n_qblocks;      /* ceil(N / block_size) */
+    int64_t nnz;            /* live (query block, key block) pairs */
+    int64_t live_pairs;     /* live (query token, key token) pairs */
+    int32_t n_segments;     /* groups of consecutive frames sharing one key-run list */
+    int32_t n_units;        /* attention work units per head (pairs of 128-row query tiles) */
+    int32_t n_classes;      /* cost classes of the units (longest first) */
+    const int32_t *d_row_ptr;    /* [n_qblocks + 1] CSR row offsets */
+    const int32_t *d_col_idx;    /* [nnz] live key blocks, ascending per row */
+    const int32_t *d_frame_runs; /* [F][4]: lo0, hi0, lo1, hi1 key tokens; (0,0) = no 2nd run */
+    const int32_t *d_segments;   /* [n_segments][8]: row0, rows, lo0, hi0, lo1, hi1, ntiles, keys */
+    const int32_t *d_units;      /* [n_units]: (segment << 16) | tile pair, longest first */
+    const int32_t *d_class_off;  /* [n_classes + 1] unit offsets of the cost classes */
+} vdit_plan_info;
+
+/* Build the block schedule of the frame-window + reference-frame mask
+ * ("Deleting the Mask", Fig. 3).
+ *   num_frames F >= 1, tokens_per_frame T >= 1, window_radius W >= 0,
+ *   ref_frame in [-1, F-1] (-1 = no reference frame),
+ *   block_size bs: a multiple of 16; it must divide T unless the mask is dense
+ *   (W >= F-1), where a ragged last block is allowed. F*T < 2^31.
+ * Allocates the plan's device buffers, launches the schedule kernels on
+ * `stream`, and synchronises once to read the counts. *out receives the plan
+ * (NULL on error). Errors: VDIT_ERR_INVALID (argument), VDIT_ERR_NOMEM,
+ * VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_attn_plan(int32_t num_frames, int32_t tokens_per_frame, int32_t window_radius,
+                           int32_t ref_frame, int32_t block_size, void *stream, vdit_plan **out);
+
+/* Re-launch the schedule kernels into the plan's existing buffers on `stream`
+ * (asynchronous, no allocation, no synchronisation). The contents equal those
+ * written by vdit_attn_plan. Errors: VDIT_ERR_INVALID (null plan), VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_plan_rebuild(vdit_plan *plan, void *stream);
+
+/* Fill *info with the plan's counts and device pointers. */
+VDIT_API vdit_status vdit_plan_get_info(const vdit_plan *plan, vdit_plan_info *info);
+
+/* Synchronise `stream`, then report and clear the plan's device status word,
+ * which a kernel launched with this plan sets when one of its bounded waits
+ * expires. *code receives the raw word (0 = none). Returns VDIT_OK when the
+ * word was 0, VDIT_ERR_TIMEOUT otherwise. */
+VDIT_API vdit_status vdit_plan_status(vdit_plan *plan, void *stream, int32_t *code);
+
+/* Free the plan and its device buffers (synchronous w.r.t. the device). NULL is ignored. */
+VDIT_API void vdit_plan_destroy(vdit_plan *plan);
+
+/* Bytes of device workspace vdit_key_stats needs for these sizes. */
+VDIT_API size_t vdit_key_stats_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D);
+
+/* Per-head key statistics and static-max eligibility ("Unchaining the Softmax"):
+ *   k_mean[b,h,:]  = c   = (1/N) sum_j k_j                       fp32 [B, H, D]
+ *   k_rmax[b,h]    = R   = max_j |k_j - c|_2                     fp32 [B, H]
+ *   q_nmax[b,h]    = Qm  = max_i |q_i|_2                         fp32 [B, H]
+ *   gap_bound[b,h] = G   = 2 * scale * Qm * R                    fp32 [B, H]
+ *   eligible[b,h]  = (G <= tau) ? 1 : 0                          uint8 [B, H]
+ * G bounds, for every row and every mask, how far the row's static bound can
+ * sit above its true max logit; tau = 64 keeps every row's largest term above
+ * e^-64, far from fp32 underflow. q, k: bf16 device tensors (see conventions).
+ * workspace: device buffer of at least vdit_key_stats_workspace_size bytes,
+ * caller-owned, contents need not be initialised. Reductions run in a fixed
+ * order: results are bitwise reproducible. Outputs are dense, caller-owned
+ * device arrays. Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, int32_t H, int32_t N,
+                           int32_t D, const int64_t q_strides[3], const int64_t k_strides[3],
+                           float scale, float tau, float *k_mean, float *k_rmax, float *q_nmax,
+                           float *gap_bound, uint8_t *eligible, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* The attention ("Deleting the Mask" + "Unchaining the Softmax"): for every
+ * query token i of every head,
+ *   O_i   = sum_{j in J(i)} softmax_j(scale * q_i . k_j) v_j
+ *   LSE_i = ln sum_{j in J(i)} exp(scale * q_i . k_j)
+ * with J(i) the plan's live keys. q, k, v: bf16 [B, H, N, D] device tensors,
+ * N = the plan's num_tokens. o: [B, H, N, D], bf16 (o_dtype = VDIT_O_BF16) or
+ * fp32 (VDIT_O_F32), with its own strides. lse: fp32 [B, H, N] dense, or NULL.
+ * mode: VDIT_MODE_AUTO uses the static bound on heads with eligible[b,h] != 0
+ * and online softmax elsewhere; FORCE_ONLINE uses online softmax everywhere
+ * (k_mean, k_rmax, eligible may be NULL); FORCE_STATIC uses the bound on every
+ * head (eligible may be NULL; on ineligible heads terms may underflow).
+ * k_mean, k_rmax: outputs of vdit_key_stats for the same k. A kernel whose
+ * bounded wait expires stops early and sets the plan's status word (see
+ * vdit_plan_status). The result is deterministic: two identical calls write
+ * identical bytes. Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k, const void *v,
+                          void *o, int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
+                          const int64_t q_strides[3], const int64_t k_strides[3],
+                          const int64_t v_strides[3], const int64_t o_strides[3], float scale,
+                          const float *k_mean, const float *k_rmax, const uint8_t *eligible,
+                          int32_t mode, void *stream);
+
+/* Thread-local, library-owned text of the last error on this thread ("" if none). */
+VDIT_API const char *vdit_last_error(void);
+
+/* Library version string. */
+VDIT_API const char *vdit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VDIT_H */

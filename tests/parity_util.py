@@ -1,0 +1,53 @@
+"""Shared helpers for the GPU parity tests: row sampling and the tolerance
+checks. The expected values always come from the fp64 oracle."""
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerances for attention outputs against fp64 with bf16 inputs and fp32
+# accumulation: max-abs 1e-2, mean-abs 1e-3; LSE 1e-3 absolute.
+O_MAX_ABS = 1e-2
+O_MEAN_ABS = 1e-3
+LSE_ABS = 1e-3
+
+
+def stratified_rows(w, per_frame_random=13, seed=1234):
+    """Flattened row indices ((b*H + h)*N + i): per (b, h, frame) the frame's
+    first and last row, the first row of its last 128-row tile (shifted to end
+    at the frame end), and `per_frame_random` seeded uniform rows."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    seg = w.N if w.dense else w.T            # rows sharing one key-run list
+    nseg = w.N // seg
+    for bh in range(w.B * w.H):
+        for s in range(nseg):
+            lo, hi = s * seg, (s + 1) * seg
+            picks = {lo, hi - 1, max(lo, hi - 128)}
+            picks.update(int(x) for x in rng.integers(lo, hi, per_frame_random))
+            rows.extend(bh * w.N + i for i in sorted(picks))
+    return np.array(rows, dtype=np.int64)
+
+
+def oracle_rows(w, q, k, v, rows=None):
+    return oracle.attention_rows(q, k, v, w.T, w.W, w.ref, w.scale, rows)
+
+
+def gather_rows(t, rows, N):
+    """t: [B, H, N, D] or [B, H, N] CUDA tensor -> numpy float64 of the given flat rows."""
+    if t.dim() == 4:
+        flat = t.reshape(-1, t.shape[-1])
+    else:
+        flat = t.reshape(-1)
+    idx = torch.from_numpy(rows).to(t.device)
+    return flat.index_select(0, idx).double().cpu().numpy()
+
+
+def check_close(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
+    err = np.abs(o_gpu - o_ref)
+    assert err.max() <= O_MAX_ABS, f"{what}: max-abs {err.max():.3e} > {O_MAX_ABS}"
+    assert err.mean() <= O_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e} > {O_MEAN_ABS}"
+    if lse_gpu is not None:
+        e2 = np.abs(lse_gpu - lse_ref)
+        assert e2.max() <= LSE_ABS, f"{what}: lse max-abs {e2.max():.3e} > {LSE_ABS}"
+    return float(err.max()), float(err.mean())

@@ -1,0 +1,102 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every entry
+point include/vdit.h declares, and rejects bad arguments on the host before
+touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_video_frame_gb300 as vd
+from block_sparse_video_frame_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "vdit.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return vd.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"VDIT_API\s+[\w\s\*]*?\b(vdit_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert set(names) == set(vd.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert "sm_103a" in vd.version()
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((4, 48, 1, 0, 15), "multiple of 16"),
+    ((4, 48, 1, 0, 0), "multiple of 16"),
+    ((4, 50, 1, 0, 16), "does not divide"),
+    ((9, 400, 1, 0, 128), "does not divide"),
+    ((0, 48, 1, 0, 16), "num_frames"),
+    ((4, 0, 1, 0, 16), "tokens_per_frame"),
+    ((4, 48, -1, 0, 16), "window_radius"),
+    ((4, 48, 1, 4, 16), "ref_frame"),
+    ((4, 48, 1, -2, 16), "ref_frame"),
+    ((5000, 48, 1, 0, 16), "num_frames"),
+    ((2, 1 << 30, 1, 0, 16), "int32"),
+])
+def test_plan_rejects_bad_arguments(lib, args, needle):
+    h = ctypes.c_void_p(1234)
+    st = lib.vdit_attn_plan(*args, None, ctypes.byref(h))
+    assert st == vd.VDIT_ERR_INVALID
+    assert needle in lib.vdit_last_error().decode()
+    assert not h.value
+
+
+def test_plan_null_out(lib):
+    assert lib.vdit_attn_plan(4, 48, 1, 0, 16, None, None) == vd.VDIT_ERR_INVALID
+
+
+def test_key_stats_rejects_bad_arguments(lib):
+    s3 = vd._I64x3(8 * 128, 128 * 16, 128)
+    p = ctypes.c_void_p(0x1000)
+    ws = lib.vdit_key_stats_workspace_size(1, 2, 16, 128)
+    assert ws == 2 * 1 * (128 + 2) * 4
+    args = [p, p, 1, 2, 16, 128, s3, s3, 0.1, 64.0, p, p, p, p, p, p, ws, None]
+    bad = list(args); bad[0] = None
+    assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+    bad = list(args); bad[5] = 96
+    assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_UNSUPPORTED
+    bad = list(args); bad[16] = ws - 1
+    assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+    assert "workspace" in lib.vdit_last_error().decode()
+    bad = list(args); bad[0] = ctypes.c_void_p(0x1008)
+    assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+    bad = list(args); bad[6] = vd._I64x3(8 * 128, 128 * 16, 100)
+    assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+
+
+def test_attn_fwd_rejects_null_plan(lib):
+    s3 = vd._I64x3(8, 8, 8)
+    p = ctypes.c_void_p(0x1000)
+    st = lib.vdit_attn_fwd(None, p, p, p, p, 0, None, 1, 1, 128, s3, s3, s3, s3, 0.1, p, p, p, 0, None)
+    assert st == vd.VDIT_ERR_INVALID
+    assert "plan" in lib.vdit_last_error().decode()
+
+
+def test_product_path_does_not_import_oracle():
+    """The library package never reaches the oracle (no CPU fallback)."""
+    pkg = os.path.dirname(vd.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "vdit_oracle" not in text, f

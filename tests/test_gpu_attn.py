@@ -1,0 +1,148 @@
+"""GPU parity of the fused attention against the fp64 oracle.
+
+Full-row comparisons on cases the oracle finishes in seconds (several query and
+key tiles, ragged key tails, segments shorter than a tile, dense with a key
+count that is not a multiple of 16, no reference frame, reference frame in the
+middle, D = 64 and 128, batch > 1, strided inputs); stratified row samples at
+the full 720p-like, 1080p-like and dense sizes in the launch configuration the
+benchmark times. Tolerances: max-abs 1e-2, mean-abs 1e-3 on O (fp32 output),
+1e-3 on LSE; the bf16 output equals the fp32 output rounded to nearest even.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_video_frame_gb300 as vd
+from block_sparse_video_frame_gb300 import configs, synth
+
+from parity_util import check_close, gather_rows, oracle_rows, stratified_rows
+
+pytestmark = pytest.mark.gpu
+
+SMALL_CASES = [
+    configs.TINY,
+    configs.SMALL,
+    configs.SMALL.with_(name="small_bs16", block_size=16),
+    configs.TINY.with_(name="tiny_d128", D=128, H=3, outlier_heads=(2,)),
+    configs.Workload("noref_w0", B=1, H=2, D=128, F=6, T=160, W=0, ref=-1, block_size=32,
+                     outlier_heads=(1,), seed=11),
+    configs.Workload("ref_mid", B=2, H=2, D=128, F=7, T=144, W=1, ref=3, block_size=48,
+                     outlier_heads=(0,), seed=12),
+    configs.Workload("dense_tail8", B=1, H=2, D=128, F=21, T=104, W=20, ref=0, block_size=16,
+                     outlier_heads=(1,), seed=13),
+    configs.Workload("dense_tiny", B=1, H=2, D=64, F=5, T=24, W=4, ref=0, block_size=16,
+                     outlier_heads=(), seed=14),
+    configs.Workload("one_frame", B=1, H=2, D=128, F=1, T=400, W=0, ref=0, block_size=16,
+                     outlier_heads=(1,), seed=15),
+    configs.Workload("wide_w", B=1, H=2, D=64, F=10, T=64, W=3, ref=0, block_size=64,
+                     outlier_heads=(1,), seed=16),
+]
+
+
+def run_gpu(w, q, k, v, mode="auto", out_dtype=torch.float32, stats=None):
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    qd, kd, vd_ = q.cuda(), k.cuda(), v.cuda()
+    if stats is None:
+        stats = vd.key_stats(qd, kd, w.scale)
+    o, lse = vd.attn_fwd(plan, qd, kd, vd_, stats, w.scale, mode=mode, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    return o, lse, stats, plan
+
+
+@pytest.mark.parametrize("w", SMALL_CASES, ids=lambda w: w.name)
+def test_attention_full_rows(w):
+    q, k, v = synth.make_qkv(w)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v)
+    o, lse, st, _ = run_gpu(w, q, k, v)
+    check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref,
+                lse.reshape(-1).double().cpu().numpy(), lse_ref, w.name)
+    # the outlier heads are the ineligible ones (they took the online branch)
+    elig = st["eligible"].cpu().numpy()
+    for h in range(w.H):
+        assert elig[:, h].all() == (h not in w.outlier_heads)
+
+
+@pytest.mark.parametrize("w", SMALL_CASES[:3] + SMALL_CASES[5:7], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", ["online", "static"])
+def test_forced_modes_agree(w, mode):
+    """FORCE_ONLINE everywhere and FORCE_STATIC on eligible heads match the oracle."""
+    q, k, v = synth.make_qkv(w)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v)
+    o, lse, st, _ = run_gpu(w, q, k, v, mode=mode)
+    o = o.double().cpu().numpy()
+    lse = lse.double().cpu().numpy()
+    o_ref = o_ref.reshape(o.shape)
+    lse_ref = lse_ref.reshape(lse.shape)
+    heads = range(w.H) if mode == "online" else [h for h in range(w.H) if h not in w.outlier_heads]
+    for h in heads:
+        check_close(o[:, h], o_ref[:, h], lse[:, h], lse_ref[:, h], f"{w.name} {mode} h{h}")
+
+
+def test_bf16_output_is_rounded_fp32_output():
+    w = configs.SMALL
+    q, k, v = synth.make_qkv(w)
+    o32, _, st, plan = run_gpu(w, q, k, v, out_dtype=torch.float32)
+    o16, _ = vd.attn_fwd(plan, q.cuda(), k.cuda(), v.cuda(), st, w.scale, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_deterministic_bytes():
+    """Two identical calls write identical bytes (the pages' 'dual baseline')."""
+    w = configs.SMALL
+    q, k, v = synth.make_qkv(w)
+    o1, l1, st, plan = run_gpu(w, q, k, v, out_dtype=torch.bfloat16)
+    o2, l2 = vd.attn_fwd(plan, q.cuda(), k.cuda(), v.cuda(), st, w.scale, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_strided_inputs_and_outputs():
+    """[B, N, H, D] storage viewed as [B, H, N, D] for Q, K, V and O."""
+    w = configs.SMALL.with_(B=2, H=4, outlier_heads=(3,))
+    q, k, v = synth.make_qkv(w)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    perm = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    qd, kd, vd_ = perm(q), perm(k), perm(v)
+    out = torch.empty((w.B, w.N, w.H, w.D), dtype=torch.float32, device="cuda").permute(0, 2, 1, 3)
+    st = vd.key_stats(qd, kd, w.scale)
+    o, lse = vd.attn_fwd(plan, qd, kd, vd_, st, w.scale, out=out)
+    torch.cuda.synchronize()
+    check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref,
+                lse.reshape(-1).double().cpu().numpy(), lse_ref, "strided")
+
+
+def test_lse_optional():
+    w = configs.TINY
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    st = vd.key_stats(q.cuda(), k.cuda(), w.scale)
+    o, lse = vd.attn_fwd(plan, q.cuda(), k.cuda(), v.cuda(), st, w.scale, with_lse=False,
+                         out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert lse is None
+    o_ref, _, _ = oracle_rows(w, q, k, v)
+    check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref, what="no-lse")
+
+
+@pytest.mark.parametrize("w", [configs.SR720, configs.SR1080, configs.DENSE], ids=lambda w: w.name)
+def test_full_size_sampled_rows(w):
+    """Full-size workloads in the benchmark's launch configuration (AUTO mode,
+    bf16 output as timed, fp32 output for the gate), on stratified row samples."""
+    q, k, v = synth.make_qkv(w)
+    rows = stratified_rows(w)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v, rows)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    qd, kd, vd_ = q.cuda(), k.cuda(), v.cuda()
+    st = vd.key_stats(qd, kd, w.scale)
+    o32, lse = vd.attn_fwd(plan, qd, kd, vd_, st, w.scale, out_dtype=torch.float32)
+    o16, _ = vd.attn_fwd(plan, qd, kd, vd_, st, w.scale, out_dtype=torch.bfloat16, with_lse=False)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    check_close(gather_rows(o32, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref, w.name)
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    # properties that hold at any size: every row finite; LSE finite
+    assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
