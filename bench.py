@@ -1,0 +1,381 @@
+#!/usr/bin/env python
+"""Benchmark of the frame-window + reference-frame block-sparse attention path.
+
+One step = the whole hot path over one batch of synthetic input: rebuild of the
+block schedule (2 kernels), per-head key statistics and eligibility (3 kernels),
+and the fused tcgen05 attention (1 kernel), with inputs resident in HBM.
+
+Metric: effective TFLOP/s on live blocks = 4 * D * live_pairs * B * H / time,
+live pairs from the schedule (dead blocks, padding and the overlap of the
+shifted last query tile are not counted). Default workload: the 720p-like
+super-resolution attention (B=1, H=24, D=128, 13 frames x 3600 tokens, window
++-2 frames plus reference frame 0). Q+K+V are 863 MB, larger than L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload sr720p]
+  python bench.py --impl reference ...     # the fp64 CPU oracle on host cores
+
+Prints exactly one JSON line on stdout (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s on live blocks, % of GB300 BF16 peak; ms per attention call"
+NOMINAL_BF16_TFLOPS = 2250.0
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+LAUNCHES_PER_STEP = 6   # plan meta + plan csr + stats pass1/pass2/finalize + attention
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="sr720p")
+    ap.add_argument("--mode", choices=["auto", "online", "static"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--traffic-bytes", type=float, default=None,
+                    help="dram bytes per attention launch from an ncu capture (reported as is)")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling (every 200 ms) around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [x for x in vis.split(",") if x.strip()] if vis else []
+        self.dev = ids[local_rank].strip() if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [l.strip().split(", ") for l in self.tmp.read().splitlines() if l.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def live_pairs_of_rows(w, rows, frame_runs):
+    """Live keys of each sampled query row, from the schedule's per-frame runs."""
+    total = 0
+    for r in rows:
+        i = int(r) % w.N
+        lo0, hi0, lo1, hi1 = frame_runs[i // w.T]
+        total += (hi0 - lo0) + (hi1 - lo1)
+    return total
+
+
+def frame_runs_closed_form(w):
+    """Per-frame key runs as token intervals (window run and, when outside it,
+    the reference frame), used only to weight the CPU sample's live pairs."""
+    runs = []
+    for f in range(w.F):
+        lo, hi = max(0, f - w.W), min(w.F - 1, f + w.W)
+        r = [[lo * w.T, (hi + 1) * w.T]]
+        if w.ref >= 0 and not lo <= w.ref <= hi:
+            r.append([w.ref * w.T, (w.ref + 1) * w.T])
+        r.sort()
+        if len(r) == 2 and r[0][1] == r[1][0]:
+            r = [[r[0][0], r[1][1]]]
+        flat = r[0] + (r[1] if len(r) > 1 else [0, 0])
+        runs.append(flat)
+    return runs
+
+
+def cpu_oracle_sample(w, q, k, v, target_s, seed=7):
+    """Time the fp64 oracle on a bounded, seeded sample of query rows; returns
+    (tflops, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    threads = oracle.set_threads(0)
+    rng = np.random.default_rng(seed)
+    runs = frame_runs_closed_form(w)
+    total = w.B * w.H * w.N
+    probe = rng.integers(0, total, 32)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.T, w.W, w.ref, w.scale, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(total, max(32, 32 * target_s / dt)))
+    rows = rng.integers(0, total, n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.T, w.W, w.ref, w.scale, rows)
+    sec = time.perf_counter() - t0
+    pairs = live_pairs_of_rows(w, rows, runs)
+    return 4.0 * w.D * pairs / sec / 1e12, sec, n, threads
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step one bounded row sample."""
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return 0
+    from block_sparse_video_frame_gb300 import configs, synth
+    import numpy as np
+    import oracle
+    w = configs.BY_NAME[args.workload]
+    q, k, v = synth.make_qkv(w)
+    threads = oracle.set_threads(0)
+    per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+    rng = np.random.default_rng(11)
+    total = w.B * w.H * w.N
+    probe = rng.integers(0, total, 16)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.T, w.W, w.ref, w.scale, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(total, max(16, 16 * per_step / dt)))
+    runs = frame_runs_closed_form(w)
+    flops, secs = 0.0, 0.0
+    for s in range(args.warmup + args.steps):
+        rows = rng.integers(0, total, n)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.T, w.W, w.ref, w.scale, rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            secs += dt
+            flops += 4.0 * w.D * live_pairs_of_rows(w, rows, runs)
+    val = flops / secs / 1e12
+    sample = f"{n} uniformly drawn query rows of {w.name} per step, fp64, OpenMP over rows"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "frames": w.F,
+            "tokens_per_frame": w.T, "window_radius": w.W, "ref_frame": w.ref,
+            "block_size": w.block_size, "outlier_heads": len(w.outlier_heads),
+            "mode": args.mode, "key_tile": 128, "query_tiles_per_cta": 2,
+            "l2": "no flush: Q+K+V inputs are larger than the 126 MB L2"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    vd.load_library()
+
+    w = configs.BY_NAME[args.workload]
+    q_h, k_h, v_h = synth.make_qkv(w, seed=w.seed + rank)
+    q_h, k_h, v_h = (t.pin_memory() for t in (q_h, k_h, v_h))
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
+    st = vd.key_stats(q, k, w.scale)
+    wsbuf = torch.empty(max(16, vd.key_stats_workspace_bytes(w.B, w.H, w.N, w.D)),
+                        dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev_a=None, ev_b=None):
+        plan.rebuild()
+        vd.key_stats(q, k, w.scale, workspace=wsbuf, out=st)
+        if ev_a is not None:
+            ev_a.record(stream)
+        vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, out=o, lse=lse)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    if plan.status() != 0:
+        raise RuntimeError("attention kernel reported an expired wait during warm-up")
+
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(*evs[i])
+    t_end.record(stream)
+    barrier()
+    clocks = clk.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    if plan.status() != 0:
+        raise RuntimeError("attention kernel reported an expired wait in the timed region")
+
+    # end to end through the public API with host buffers: H2D of Q, K, V from
+    # pinned memory, the step, D2H of O, every step
+    e2e = None
+    if not args.no_e2e:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        qe, ke, ve = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for _ in range(2):
+            qe.copy_(q_h, non_blocking=True); ke.copy_(k_h, non_blocking=True); ve.copy_(v_h, non_blocking=True)
+            vd.attn_fwd(plan, qe, ke, ve, vd.key_stats(qe, ke, w.scale, workspace=wsbuf, out=st),
+                        w.scale, mode=args.mode, out=o, lse=lse)
+            o_h.copy_(o, non_blocking=True)
+        barrier()
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ke_steps = max(3, args.steps // 5)
+        e_a.record(stream)
+        for _ in range(ke_steps):
+            qe.copy_(q_h, non_blocking=True); ke.copy_(k_h, non_blocking=True); ve.copy_(v_h, non_blocking=True)
+            plan.rebuild()
+            vd.key_stats(qe, ke, w.scale, workspace=wsbuf, out=st)
+            vd.attn_fwd(plan, qe, ke, ve, st, w.scale, mode=args.mode, out=o, lse=lse)
+            o_h.copy_(o, non_blocking=True)
+        e_b.record(stream)
+        barrier()
+        e2e_ms = e_a.elapsed_time(e_b) / ke_steps
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+        d2h = o_h.numel() * o_h.element_size()
+        e2e = {"value_ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+
+    tmax = torch.tensor([elapsed_ms, statistics.mean(attn_ms), e2e["value_ms"] if e2e else 0.0],
+                        dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    elapsed_ms, attn_avg_ms, e2e_ms = (float(x) for x in tmax.tolist())
+
+    if rank == 0:
+        peaks = load_peaks()
+        ms_step = elapsed_ms / args.steps
+        value = ws * flops / (ms_step * 1e-3) / 1e12
+        achieved = flops / (attn_avg_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V, per-head key offsets, x20 outlier keys)",
+            "config": dict(config_of(w, args), live_pairs_per_head=plan.live_pairs,
+                           flop_per_step_per_gpu=flops,
+                           pct_of_2250_tflops=100.0 * value / ws / NOMINAL_BF16_TFLOPS,
+                           attn_ms_median=statistics.median(attn_ms),
+                           attn_ms_min=min(attn_ms), attn_ms_max=max(attn_ms)),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": args.traffic_bytes,
+                         "kernel": "attn_fwd_kernel<128>", "peak_source":
+                         f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "clocks": clocks,
+        }
+        if e2e:
+            line["e2e"] = {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                           "ms_per_step": e2e_ms}
+        if ws == 1 and not args.no_cpu_baseline:
+            val, sec, n, threads = cpu_oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
+                                    "kind": "oracle", "seconds": sec,
+                                    "sample": f"{n} uniformly drawn query rows of {w.name}, "
+                                              "fp64, OpenMP over rows, all host cores"}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    plan.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

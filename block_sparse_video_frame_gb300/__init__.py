@@ -196,7 +196,7 @@ class _DeviceInts:
 
     def __init__(self, ptr, n):
         self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4",
-                                         "data": (int(ptr), True), "version": 3,
+                                         "data": (int(ptr), False), "version": 3,
                                          "strides": None}
 
 
@@ -205,9 +205,10 @@ def attn_plan(F, T, W, ref, block_size, stream=None) -> Plan:
     return Plan(F, T, W, ref, block_size, stream)
 
 
-def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None):
+def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None, out=None):
     """Per-head key mean, max centred key norm, max query norm, gap bound G and
-    eligibility G <= tau (vdit_key_stats). Returns a dict of CUDA tensors."""
+    eligibility G <= tau (vdit_key_stats). Returns a dict of CUDA tensors
+    (written into `out` when given, e.g. the dict a previous call returned)."""
     import torch
     _check_bhnd("q", q)
     _check_bhnd("k", k, q.shape[3])
@@ -218,12 +219,19 @@ def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None):
     B, H, N, D = q.shape
     lib = load_library()
     dev = q.device
-    out = dict(k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev),
-               k_rmax=torch.empty((B, H), dtype=torch.float32, device=dev),
-               q_nmax=torch.empty((B, H), dtype=torch.float32, device=dev),
-               gap=torch.empty((B, H), dtype=torch.float32, device=dev),
-               eligible=torch.empty((B, H), dtype=torch.uint8, device=dev))
-    need = lib.vdit_key_stats_workspace_size(B, H, N, D)
+    if out is None:
+        out = dict(k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev),
+                   k_rmax=torch.empty((B, H), dtype=torch.float32, device=dev),
+                   q_nmax=torch.empty((B, H), dtype=torch.float32, device=dev),
+                   gap=torch.empty((B, H), dtype=torch.float32, device=dev),
+                   eligible=torch.empty((B, H), dtype=torch.uint8, device=dev))
+    for name, shape, dt in (("k_mean", (B, H, D), torch.float32), ("k_rmax", (B, H), torch.float32),
+                            ("q_nmax", (B, H), torch.float32), ("gap", (B, H), torch.float32),
+                            ("eligible", (B, H), torch.uint8)):
+        t = out[name]
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"key_stats out[{name!r}] must be a contiguous {dt} {shape} tensor on {dev}")
+    need = key_stats_workspace_bytes(B, H, N, D)
     if workspace is None:
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
     _check(lib.vdit_key_stats(_ptr(q), _ptr(k), B, H, N, D, _strides(q), _strides(k),
@@ -232,6 +240,10 @@ def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None):
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream)))
     return out
+
+
+def key_stats_workspace_bytes(B, H, N, D) -> int:
+    return int(load_library().vdit_key_stats_workspace_size(int(B), int(H), int(N), int(D)))
 
 
 def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype=None,

@@ -59,7 +59,10 @@ DENSE = Workload("dense_base", B=1, H=24, D=128, F=21, T=1560, W=20, ref=0, bloc
                  outlier_heads=(18, 19, 20, 21, 22, 23), seed=4)
 
 ALL = (TINY, SMALL, SR720, SR1080, DENSE)
-BY_NAME = {w.name: w for w in ALL}
+# 720p-like geometry with 8 heads (Q+K+V = 288 MB, still larger than L2): the
+# case profiled with the full ncu section set.
+SR720_H8 = SR720.with_(name="sr720p_h8", H=8, outlier_heads=(7,))
+BY_NAME = {w.name: w for w in ALL + (SR720_H8,)}
 
 
 def dense_sweep():
