@@ -25,7 +25,7 @@ VDIT_OK, VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA, VDIT_ERR_NOMEM, 
 MODES = {"auto": 0, "online": 1, "static": 2}
 EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_plan_status",
             "vdit_plan_destroy", "vdit_key_stats_workspace_size", "vdit_key_stats",
-            "vdit_attn_fwd", "vdit_last_error", "vdit_version")
+            "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc")
 
 
 class VditError(RuntimeError):

@@ -15,6 +15,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "vdit_internal.h"
 
 namespace vdit {
@@ -228,6 +230,122 @@ extern "C" vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, i
     a.scale = scale; a.tau = tau;
     const size_t slots = (size_t)B * H * a.nchunk;
     a.ws_colsum = static_cast<float *>(workspace);
+    a.ws_qn2 = a.ws_colsum + slots * D;
+    a.ws_rn2 = a.ws_qn2 + slots;
+    a.k_mean = k_mean; a.k_rmax = k_rmax; a.q_nmax = q_nmax; a.gap = gap_bound;
+    a.elig = eligible;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dim3 grid(a.nchunk, B * H);
+    if (D == 128) {
+        stats_pass1<128><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_pass2<128><<<grid, kStatsThreads, 0, s>>>(a);
+    } else {
+        stats_pass1<64><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
+    }
+    stats_finalize<<<B * H, 32, 0, s>>>(a);
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of vdit_key_stats.
+//
+// Some callers cannot allocate device memory: a plugin whose host framework
+// owns every device buffer through its own pool and forbids plugins from
+// calling cudaMalloc, or a latency-critical loop that must not pay
+// cudaMalloc's implicit device-wide synchronisation after start-up. This entry
+// point runs the same three kernels as vdit_key_stats, but takes their scratch
+// from a fixed array compiled into the library instead of from a caller buffer.
+//
+// The array below lives in device memory for as long as the library stays
+// loaded, on every GPU that loads it. Every call shares it and it keeps the
+// previous call's contents; the kernels overwrite every scratch slot they read
+// (nothing needs to start at zero). Two calls whose kernels overlap on the GPU
+// (e.g. on different streams, or on one device from several host threads
+// without ordering) race on the array.
+namespace vdit {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_key_stats_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, not a device address).
+cudaError_t scratch_address(int device, void **out) {
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_scratch_addr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_key_stats_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[device] = p;
+    }
+    *out = g_scratch_addr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace vdit
+
+extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int32_t B, int32_t H,
+                                              int32_t N, int32_t D, const int64_t q_strides[3],
+                                              const int64_t k_strides[3], float scale, float tau,
+                                              float *k_mean, float *k_rmax, float *q_nmax,
+                                              float *gap_bound, uint8_t *eligible, void *stream) {
+    clear_error();
+    if (!q || !k || !q_strides || !k_strides || !k_mean || !k_rmax || !q_nmax || !gap_bound ||
+        !eligible) {
+        set_error("vdit_key_stats_noalloc: NULL pointer argument");
+        return VDIT_ERR_INVALID;
+    }
+    if (B < 1 || H < 1 || N < 1) {
+        set_error("vdit_key_stats_noalloc: B=%d H=%d N=%d must be >= 1", B, H, N);
+        return VDIT_ERR_INVALID;
+    }
+    if (D != 64 && D != 128) {
+        set_error("vdit_key_stats_noalloc: head dim D=%d not supported (64 or 128)", D);
+        return VDIT_ERR_UNSUPPORTED;
+    }
+    for (int i = 0; i < 3; ++i) {
+        if (q_strides[i] <= 0 || k_strides[i] <= 0 || q_strides[i] % 8 || k_strides[i] % 8) {
+            set_error("vdit_key_stats_noalloc: strides must be positive multiples of 8 elements");
+            return VDIT_ERR_INVALID;
+        }
+    }
+    if (!aligned16(q) || !aligned16(k)) {
+        set_error("vdit_key_stats_noalloc: q and k must be 16-byte aligned");
+        return VDIT_ERR_INVALID;
+    }
+    if (!(scale > 0.f) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats_noalloc: scale must be > 0 and tau >= 0");
+        return VDIT_ERR_INVALID;
+    }
+    const size_t need = vdit_key_stats_workspace_size(B, H, N, D);
+    if (need > kNoAllocScratchBytes) {
+        set_error("vdit_key_stats_noalloc: these sizes need %zu bytes of scratch, more than the "
+                  "built-in %zu bytes (B*H*ceil(N/1024)*(D+2)*4 must not exceed it); use "
+                  "vdit_key_stats with a caller workspace", need, kNoAllocScratchBytes);
+        return VDIT_ERR_INVALID;
+    }
+    int dev = -1;
+    VDIT_CUDA_TRY(cudaGetDevice(&dev));
+    void *scratch = nullptr;
+    cudaError_t e = scratch_address(dev, &scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "vdit_key_stats_noalloc: cudaGetSymbolAddress");
+    StatsArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.qs0 = q_strides[0]; a.qs1 = q_strides[1]; a.qs2 = q_strides[2];
+    a.ks0 = k_strides[0]; a.ks1 = k_strides[1]; a.ks2 = k_strides[2];
+    a.B = B; a.H = H; a.N = N; a.nchunk = nchunks(N);
+    a.scale = scale; a.tau = tau;
+    const size_t slots = (size_t)B * H * a.nchunk;
+    a.ws_colsum = static_cast<float *>(scratch);
     a.ws_qn2 = a.ws_colsum + slots * D;
     a.ws_rn2 = a.ws_qn2 + slots;
     a.k_mean = k_mean; a.k_rmax = k_rmax; a.q_nmax = q_nmax; a.gap = gap_bound;

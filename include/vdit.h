@@ -133,6 +133,26 @@ VDIT_API vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, int
                            float *gap_bound, uint8_t *eligible, void *workspace,
                            size_t workspace_bytes, void *stream);
 
+/* Allocation-free vdit_key_stats. The source pages have no counterpart to this
+ * entry point; it exists for callers that may not allocate device memory at
+ * all: plugins whose host framework owns every device buffer and forbids
+ * cudaMalloc, or latency-critical loops that cannot afford cudaMalloc's
+ * implicit device synchronisation. Same arguments, outputs and results as
+ * vdit_key_stats, without the workspace: the scratch comes from a 4 MiB array
+ * compiled into the library, resident on every GPU that loads it until the
+ * process exits. Sizes with B*H*ceil(N/1024)*(D+2)*4 > 4 MiB are rejected with
+ * VDIT_ERR_INVALID before any launch. The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the array
+ * and it keeps the last call's contents (every slot is rewritten before it is
+ * read); calls whose kernels overlap on the GPU race on it and must be
+ * ordered by the caller. Calls no cudaMalloc/cudaFree. */
+VDIT_API vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int32_t B, int32_t H,
+                                            int32_t N, int32_t D, const int64_t q_strides[3],
+                                            const int64_t k_strides[3], float scale, float tau,
+                                            float *k_mean, float *k_rmax, float *q_nmax,
+                                            float *gap_bound, uint8_t *eligible, void *stream);
+
 /* The attention ("Deleting the Mask" + "Unchaining the Softmax"): for every
  * query token i of every head,
  *   O_i   = sum_{j in J(i)} softmax_j(scale * q_i . k_j) v_j
