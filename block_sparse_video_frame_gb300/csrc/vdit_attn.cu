@@ -43,7 +43,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kBK = 128;              // keys per K/V tile
-constexpr int kStages = 2;            // K and V ring depth
+constexpr int kStagesK = 2;           // K ring depth (a K tile is free once its S MMAs finish)
+constexpr int kStagesV = 3;           // V ring depth (V is held until P.V finishes)
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
@@ -62,8 +63,8 @@ struct Layout {
     static constexpr int kTileBytes = kTileRows * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTilesPerUnit * kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kBar = kV + kStages * kTileBytes;
+    static constexpr int kV = kK + kStagesK * kTileBytes;
+    static constexpr int kBar = kV + kStagesV * kTileBytes;
     static constexpr int kBytes = kBar + 256;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemO = 0;         // O0 at col 0, O1 at col D
@@ -72,9 +73,9 @@ struct Layout {
 
 // barrier slots (8 bytes each) after the tiles
 enum : int {
-    kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = 4, kBarVfull = 6, kBarVfree = 8,
-    kBarSfull = 10, kBarPfull = 12, kBarOfull = 14, kBarOfree = 16, kBarFinal = 18,
-    kNumBars = 19
+    kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = 4, kBarVfull = 6, kBarVfree = 9,
+    kBarSfull = 12, kBarPfull = 14, kBarOfull = 16, kBarOfree = 18, kBarFinal = 20,
+    kNumBars = 21
 };
 
 struct Params {
@@ -176,9 +177,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQfull), 1);
         mbar_init(bar(kBarQfree), 1 + 8);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStagesK; ++s) {
             mbar_init(bar(kBarKfull + s), 1);
             mbar_init(bar(kBarKfree + s), 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
             mbar_init(bar(kBarVfull + s), 1);
             mbar_init(bar(kBarVfree + s), 1);
         }
@@ -227,126 +230,146 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int j = 0; j < u.nkt; ++j) {
                     int start, nvalid;
                     key_tile(u, j, start, nvalid);
-                    const int st = nk % kStages;
-                    const uint32_t par = ((nk / kStages) & 1) ^ 1;
-                    if (!(ok = mbar_wait(bar(kBarKfree + st), par, abort_flag, p.status, kSiteKfree, tlim)))
+                    const int sk = nk % kStagesK;
+                    if (!(ok = mbar_wait(bar(kBarKfree + sk), ((nk / kStagesK) & 1) ^ 1, abort_flag,
+                                         p.status, kSiteKfree, tlim)))
                         break;
-                    mbar_arrive_expect_tx(bar(kBarKfull + st), L::kTileBytes);
+                    mbar_arrive_expect_tx(bar(kBarKfull + sk), L::kTileBytes);
                     for (int hf = 0; hf < D / 64; ++hf)
-                        tma_load_4d(sbase + L::kK + st * L::kTileBytes + hf * kHalfBytes, &tm_k,
-                                    bar(kBarKfull + st), hf * 64, start, u.h, u.b);
+                        tma_load_4d(sbase + L::kK + sk * L::kTileBytes + hf * kHalfBytes, &tm_k,
+                                    bar(kBarKfull + sk), hf * 64, start, u.h, u.b);
                     ++nk;
-                    if (!(ok = mbar_wait(bar(kBarVfree + st), par, abort_flag, p.status, kSiteVfree, tlim)))
+                    const int sv = nv % kStagesV;
+                    if (!(ok = mbar_wait(bar(kBarVfree + sv), ((nv / kStagesV) & 1) ^ 1, abort_flag,
+                                         p.status, kSiteVfree, tlim)))
                         break;
-                    mbar_arrive_expect_tx(bar(kBarVfull + st), L::kTileBytes);
+                    mbar_arrive_expect_tx(bar(kBarVfull + sv), L::kTileBytes);
                     for (int hf = 0; hf < D / 64; ++hf)
-                        tma_load_4d(sbase + L::kV + st * L::kTileBytes + hf * kHalfBytes, &tm_v,
-                                    bar(kBarVfull + st), hf * 64, start, u.h, u.b);
+                        tma_load_4d(sbase + L::kV + sv * L::kTileBytes + hf * kHalfBytes, &tm_v,
+                                    bar(kBarVfull + sv), hf * 64, start, u.h, u.b);
                     ++nv;
                 }
             }
             // drain: every copy this thread issued must land before the CTA exits
-            for (int s = 0; s < kStages; ++s) {
-                const uint32_t n_k = nk / kStages + ((uint32_t)s < nk % kStages ? 1u : 0u);
-                const uint32_t n_v = nv / kStages + ((uint32_t)s < nv % kStages ? 1u : 0u);
+            for (int s = 0; s < kStagesK; ++s) {
+                const uint32_t n_k = nk / kStagesK + ((uint32_t)s < nk % kStagesK ? 1u : 0u);
                 if (n_k > 0) drain_wait(bar(kBarKfull + s), (n_k - 1) & 1, tlim);
+            }
+            for (int s = 0; s < kStagesV; ++s) {
+                const uint32_t n_v = nv / kStagesV + ((uint32_t)s < nv % kStagesV ? 1u : 0u);
                 if (n_v > 0) drain_wait(bar(kBarVfull + s), (n_v - 1) & 1, tlim);
             }
             if (it > 0) drain_wait(bar(kBarQfull), (it - 1) & 1, tlim);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_pv = idesc_bf16(128, D, true);
-            uint32_t kc = 0, it = 0, sq[kTilesPerUnit] = {0, 0}, uq[kTilesPerUnit] = {0, 0};
-            bool ok = true;
-            auto issue_s = [&](int q, int st, int nmma) {
-                const uint32_t idesc = idesc_bf16(128, nmma, false);
-                const uint32_t qa = sbase + L::kQ + q * L::kTileBytes;
-                const uint32_t ka = sbase + L::kK + st * L::kTileBytes;
+        // The whole warp walks the schedule (warp-uniform control flow) and one
+        // elected lane issues every tcgen05.mma and commit. A tcgen05.mma issue
+        // returns only when the tensor pipe can take it, so anything computed
+        // between two MMAs is idle tensor time: descriptors are built once and
+        // K-steps add compile-time offsets to the start-address field.
+        const bool leader = elect_one();
+        constexpr uint32_t kTileDesc = L::kTileBytes >> 4;   // one tile, in descriptor address units
+        const uint64_t dQ = sdesc_sw128(sbase + L::kQ, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sbase + L::kK, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sbase + L::kV, kHalfBytes, 1024);
+        const uint32_t tS0 = tmem + L::kTmemS, tO0 = tmem + L::kTmemO;
+        constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
+        constexpr uint32_t kIdescS = idesc_bf16(128, kBK, false);
+        // S_q = Q_q K^T (K-major A and B); a tail tile uses a narrower N
+        auto issue_s = [&](int q, int sk, int nmma) {
+            const uint64_t a0 = dQ + (uint64_t)(q * kTileDesc);
+            const uint64_t b0 = dK + (uint64_t)(sk * kTileDesc);
+            const uint32_t idesc = nmma == kBK ? kIdescS : idesc_bf16(128, nmma, false);
+            const uint32_t d = tS0 + q * 128;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                    mma_ss(tmem + L::kTmemS + q * 128, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), idesc, ks > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int q, int st, int nmma, bool acc) {
-                const uint32_t va = sbase + L::kV + st * L::kTileBytes;
-                for (int ks = 0; ks < nmma / 16; ++ks) {
-                    mma_ts(tmem + L::kTmemO + q * D, tmem + L::kTmemS + q * 128 + ks * 8,
-                           sdesc_sw128(va + ks * 2048, kHalfBytes, 1024), idesc_pv,
-                           (acc || ks > 0) ? 1u : 0u);
-                }
-            };
-            for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
-                Work u;
-                decode(p, w, u);
-                if (!(ok = mbar_wait(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullMma, tlim)))
-                    break;
-                const uint32_t kc0 = kc;
-                int start, nvalid;
-                key_tile(u, 0, start, nvalid);
-                {
-                    const int st = kc0 % kStages;
-                    if (!(ok = mbar_wait(bar(kBarKfull + st), (kc0 / kStages) & 1, abort_flag, p.status,
-                                         kSiteKfull, tlim)))
-                        break;
-                    tc_fence_after();
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks / 4) * (kHalfBytes >> 4) + (ks % 4) * 2;
+                mma_ss(d, a0 + off, b0 + off, idesc, ks > 0 ? 1u : 0u);
+            }
+        };
+        // O_q (+)= P_q V: P from TMEM (8 packed columns per 16 keys), V MN-major
+        auto issue_pv = [&](int q, int sv, int nmma, bool acc) {
+            const uint64_t b0 = dV + (uint64_t)(sv * kTileDesc);
+            const uint32_t d = tO0 + q * D, a = tS0 + q * 128;
+#pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+                if (ks * 16 < nmma)
+                    mma_ts(d, a + ks * 8, b0 + ks * (2048 >> 4), kIdescPV, (ks > 0 || acc) ? 1u : 0u);
+            }
+        };
+        auto wait = [&](int b, uint32_t parity, int site) {
+            const bool r = mbar_wait(bar(b), parity, abort_flag, p.status, site, tlim);
+            return __all_sync(0xffffffffu, r);
+        };
+        uint32_t kc = 0, it = 0, sq[kTilesPerUnit] = {0, 0}, uq[kTilesPerUnit] = {0, 0};
+        bool ok = true;
+        for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
+            Work u;
+            decode(p, w, u);
+            if (!(ok = wait(kBarQfull, it & 1, kSiteQfullMma))) break;
+            const uint32_t kc0 = kc;
+            int start, nvalid;
+            key_tile(u, 0, start, nvalid);
+            {
+                const int sk = kc0 % kStagesK;
+                if (!(ok = wait(kBarKfull + sk, (kc0 / kStagesK) & 1, kSiteKfull))) break;
+                tc_fence_after();
+                if (leader) {
                     for (int q = 0; q < u.nact; ++q) {
-                        issue_s(q, st, (nvalid + 15) & ~15);
+                        issue_s(q, sk, (nvalid + 15) & ~15);
                         mma_commit(bar(kBarSfull + q));
                     }
-                    mma_commit(bar(kBarKfree + st));
+                    mma_commit(bar(kBarKfree + sk));
                     if (u.nkt == 1) mma_commit(bar(kBarQfree));
                 }
-                for (int j = 0; j < u.nkt && ok; ++j) {
-                    const uint32_t c = kc0 + j;
-                    const int st = c % kStages;
-                    key_tile(u, j, start, nvalid);
-                    const int nmma = (nvalid + 15) & ~15;
-                    int start1 = 0, nvalid1 = 0;
-                    if (j + 1 < u.nkt) key_tile(u, j + 1, start1, nvalid1);
-                    if (!(ok = mbar_wait(bar(kBarVfull + st), (c / kStages) & 1, abort_flag, p.status,
-                                         kSiteVfull, tlim)))
-                        break;
-                    for (int q = 0; q < u.nact && ok; ++q) {
-                        if (!(ok = mbar_wait(bar(kBarPfull + q), sq[q] & 1, abort_flag, p.status,
-                                             kSitePfull, tlim)))
-                            break;
-                        if (j == 0 && !(ok = mbar_wait(bar(kBarOfree + q), (uq[q] & 1) ^ 1, abort_flag,
-                                                       p.status, kSiteOfree, tlim)))
-                            break;
-                        tc_fence_after();
-                        issue_pv(q, st, nmma, j > 0);
-                        ++sq[q];
-                        if (q == u.nact - 1) mma_commit(bar(kBarVfree + st));
+                __syncwarp();
+            }
+            for (int j = 0; j < u.nkt && ok; ++j) {
+                const uint32_t c = kc0 + j;
+                const int sv = c % kStagesV;
+                key_tile(u, j, start, nvalid);
+                const int nmma = (nvalid + 15) & ~15;
+                int start1 = 0, nvalid1 = 0;
+                if (j + 1 < u.nkt) key_tile(u, j + 1, start1, nvalid1);
+                const uint32_t c1 = c + 1;
+                const int sk1 = c1 % kStagesK;
+                if (!(ok = wait(kBarVfull + sv, (c / kStagesV) & 1, kSiteVfull))) break;
+                for (int q = 0; q < u.nact && ok; ++q) {
+                    if (!(ok = wait(kBarPfull + q, sq[q] & 1, kSitePfull))) break;
+                    if (j == 0 && !(ok = wait(kBarOfree + q, (uq[q] & 1) ^ 1, kSiteOfree))) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_pv(q, sv, nmma, j > 0);
+                        if (q == u.nact - 1) mma_commit(bar(kBarVfree + sv));
                         if (j == u.nkt - 1) mma_commit(bar(kBarOfull + q));
-                        if (j + 1 < u.nkt) {
-                            const uint32_t c1 = c + 1;
-                            const int st1 = c1 % kStages;
-                            if (q == 0) {
-                                if (!(ok = mbar_wait(bar(kBarKfull + st1), (c1 / kStages) & 1, abort_flag,
-                                                     p.status, kSiteKfull, tlim)))
-                                    break;
-                                tc_fence_after();
-                            }
-                            issue_s(q, st1, (nvalid1 + 15) & ~15);
+                    }
+                    __syncwarp();
+                    ++sq[q];
+                    if (j + 1 < u.nkt) {
+                        if (q == 0) {
+                            if (!(ok = wait(kBarKfull + sk1, (c1 / kStagesK) & 1, kSiteKfull))) break;
+                            tc_fence_after();
+                        }
+                        if (leader) {
+                            issue_s(q, sk1, (nvalid1 + 15) & ~15);
                             mma_commit(bar(kBarSfull + q));
                             if (q == u.nact - 1) {
-                                mma_commit(bar(kBarKfree + st1));
+                                mma_commit(bar(kBarKfree + sk1));
                                 if (j + 1 == u.nkt - 1) mma_commit(bar(kBarQfree));
                             }
                         }
+                        __syncwarp();
                     }
                 }
-                for (int q = 0; q < u.nact; ++q) ++uq[q];
-                kc += u.nkt;
             }
-            // drain: all issued MMAs complete before TMEM is released
-            mma_commit(bar(kBarFinal));
-            drain_wait(bar(kBarFinal), 0, tlim);
+            for (int q = 0; q < u.nact; ++q) ++uq[q];
+            kc += u.nkt;
         }
+        // drain: all issued MMAs complete before TMEM is released
+        if (leader) mma_commit(bar(kBarFinal));
+        __syncwarp();
+        drain_wait(bar(kBarFinal), 0, tlim);
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         const int q = warp / 4;                  // query tile of this warpgroup
