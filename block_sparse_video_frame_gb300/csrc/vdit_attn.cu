@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "vdit_internal.h"
 #include "vdit_ptx.cuh"
@@ -51,6 +52,25 @@ constexpr int kWarpMma = 9;
 constexpr int kHalfBytes = 128 * 128; // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr float kLazyRescale = 8.0f;  // online: rescale only when the max rises > 2^8
+// Of every 8 columns of S, this many take their exponential on the FMA pipe
+// (exp2_fma) instead of MUFU ex2: MUFU issues 16 ex2 per clock per SM, which
+// alone would pace the softmax below the tensor pipe.
+constexpr int kPolyPer8 = 0;
+
+template <int C>
+__device__ __forceinline__ float softmax_exp2(float x) {
+    if constexpr ((C % 8) >= 8 - kPolyPer8) return exp2_fma(x);
+    else return ex2(x);
+}
+
+// Compile-time loop: f(std::integral_constant<int, i>) for i in [0, N).
+template <int N, int I = 0, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for<N, I + 1>(f);
+    }
+}
 
 // status-word site codes (which wait expired)
 enum : int {
@@ -370,7 +390,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (leader) mma_commit(bar(kBarFinal));
         __syncwarp();
         drain_wait(bar(kBarFinal), 0, tlim);
-    } else {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ softmax warpgroups
         const int q = warp / 4;                  // query tile of this warpgroup
         const int r = threadIdx.x % kTileRows;   // row within the tile = TMEM lane
@@ -423,7 +443,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int j = 0; j < u.nkt; ++j) {
                 int start, nvalid;
                 key_tile(u, j, start, nvalid);
-                const int nmma = (nvalid + 15) & ~15;
                 ok = mbar_wait(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
@@ -431,13 +450,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!stat) {
                     // online: this tile's row max (pass 1), lazy rescale of O
                     float mx = -INFINITY;
-                    for (int c0 = 0; c0 < nmma; c0 += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(tS + c0, v);
+                    {
+                        uint32_t v[128];
+                        tmem_ld128(tS, v);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
+                        for (int e = 0; e < 128; ++e) {
                             const float x = __uint_as_float(v[e]) * sc;
-                            mx = (c0 + e < nvalid) ? fmaxf(mx, x) : mx;
+                            mx = (e < nvalid) ? fmaxf(mx, x) : mx;
                         }
                     }
                     if (j == 0) {
@@ -462,36 +481,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     mrow = mrun;
                 }
-                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S
-                for (int c0 = 0; c0 < nmma; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + c0, v);
-                    uint32_t pk[16];
-                    if (c0 + 32 <= nvalid) {
+                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S;
+                // the whole 128-column S row in one TMEM load
+                {
+                    uint32_t v[128];
+                    tmem_ld128(tS, v);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), sc, -mrow));
-                            const float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mrow));
-                            l0 += p0;
-                            l1 += p1;
-                            pk[e] = pack_bf16(p0, p1);
-                        }
-                    } else {
+                    for (int hf = 0; hf < 2; ++hf) {      // P stored 32 packed columns at a time
+                        uint32_t pk[32];
+                        if (nvalid >= kBK) {
+                            static_for<32>([&](auto E) {
+                                constexpr int e = decltype(E)::value;
+                                const int i0 = hf * 64 + 2 * e;
+                                const float p0 = softmax_exp2<2 * e>(fmaf(__uint_as_float(v[i0]), sc, -mrow));
+                                const float p1 = softmax_exp2<2 * e + 1>(fmaf(__uint_as_float(v[i0 + 1]), sc, -mrow));
+                                l0 += p0;
+                                l1 += p1;
+                                pk[e] = pack_bf16(p0, p1);
+                            });
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int col = c0 + 2 * e;
-                            const float p0 = col < nvalid
-                                                 ? ex2(fmaf(__uint_as_float(v[2 * e]), sc, -mrow))
-                                                 : 0.f;
-                            const float p1 = col + 1 < nvalid
-                                                 ? ex2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mrow))
-                                                 : 0.f;
-                            l0 += p0;
-                            l1 += p1;
-                            pk[e] = pack_bf16(p0, p1);
+                            for (int e = 0; e < 32; ++e) {
+                                const int i0 = hf * 64 + 2 * e;
+                                const float p0 = i0 < nvalid ? ex2(fmaf(__uint_as_float(v[i0]), sc, -mrow)) : 0.f;
+                                const float p1 =
+                                    i0 + 1 < nvalid ? ex2(fmaf(__uint_as_float(v[i0 + 1]), sc, -mrow)) : 0.f;
+                                l0 += p0;
+                                l1 += p1;
+                                pk[e] = pack_bf16(p0, p1);
+                            }
                         }
+                        tmem_st32(tS + hf * 32, pk);
                     }
-                    tmem_st16(tS + c0 / 2, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
