@@ -319,8 +319,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         };
         auto wait = [&](int b, uint32_t parity, int site) {
-            const bool r = mbar_wait(bar(b), parity, abort_flag, p.status, site, tlim);
-            return __all_sync(0xffffffffu, r);
+            return mbar_wait_warp(bar(b), parity, abort_flag, p.status, site, tlim);
         };
         uint32_t kc = 0, it = 0, sq[kTilesPerUnit] = {0, 0}, uq[kTilesPerUnit] = {0, 0};
         bool ok = true;
@@ -340,8 +339,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         issue_s(q, sk, (nvalid + 15) & ~15);
                         mma_commit(bar(kBarSfull + q));
                     }
-                    mma_commit(bar(kBarKfree + sk));
-                    if (u.nkt == 1) mma_commit(bar(kBarQfree));
                 }
                 __syncwarp();
             }
@@ -361,7 +358,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     if (leader) {
                         issue_pv(q, sv, nmma, j > 0);
-                        if (q == u.nact - 1) mma_commit(bar(kBarVfree + sv));
                         if (j == u.nkt - 1) mma_commit(bar(kBarOfull + q));
                     }
                     __syncwarp();
@@ -374,10 +370,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (leader) {
                             issue_s(q, sk1, (nvalid1 + 15) & ~15);
                             mma_commit(bar(kBarSfull + q));
-                            if (q == u.nact - 1) {
-                                mma_commit(bar(kBarKfree + sk1));
-                                if (j + 1 == u.nkt - 1) mma_commit(bar(kBarQfree));
-                            }
                         }
                         __syncwarp();
                     }
@@ -398,16 +390,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tS = tmem + L::kTmemS + q * 128 + lane_off;
         const uint32_t tO = tmem + L::kTmemO + q * D + lane_off;
         const float sc = p.scale_log2;
-        uint32_t it = 0, sq = 0, uq = 0;
+        uint32_t it = 0, sq = 0, uq = 0, kc = 0;
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
             decode(p, w, u);
             const bool act = q < u.nact;
+            // The last active warpgroup releases K, V and Q tiles: its S barrier for key
+            // tile j is committed after every earlier MMA of the unit (all S MMAs of
+            // tile j, all P.V MMAs of tile j-1); its O barrier covers the last P.V.
+            const bool releaser = q == u.nact - 1 && (warp % 4) == 0 && lane == 0;
+            const uint32_t kc0 = kc;
+            kc += u.nkt;
             const bool stat = p.mode == VDIT_MODE_FORCE_STATIC ||
                               (p.mode == VDIT_MODE_AUTO && p.elig[u.bh] != 0);
-            ok = mbar_wait(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait_warp(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
+            if (!ok) break;
             // row bound ("Unchaining the Softmax"): m~ = scale*log2e*(q.c + |q| R)
             float mt = 0.f;
             if (act && stat) {
@@ -443,9 +441,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int j = 0; j < u.nkt; ++j) {
                 int start, nvalid;
                 key_tile(u, j, start, nvalid);
-                ok = mbar_wait(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                ok = mbar_wait_warp(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
+                if (!ok) break;
                 tc_fence_after();
+                if (releaser) {
+                    mbar_arrive(bar(kBarKfree + (kc0 + j) % kStagesK));
+                    if (j > 0) mbar_arrive(bar(kBarVfree + (kc0 + j - 1) % kStagesV));
+                    if (j == u.nkt - 1) mbar_arrive(bar(kBarQfree));
+                }
                 float mrow = mt;
                 if (!stat) {
                     // online: this tile's row max (pass 1), lazy rescale of O
@@ -522,9 +525,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!stat) mt = mrun;
             }
             if (!ok) break;
-            ok = mbar_wait(bar(kBarOfull + q), uq & 1, abort_flag, p.status, kSiteOfull, tlim);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait_warp(bar(kBarOfull + q), uq & 1, abort_flag, p.status, kSiteOfull, tlim);
+            if (!ok) break;
             tc_fence_after();
+            if (releaser) mbar_arrive(bar(kBarVfree + (kc0 + u.nkt - 1) % kStagesV));
             // epilogue: O / l for the rows this tile owns, and LSE
             const float l = l0 + l1;
             const float inv = 1.0f / l;

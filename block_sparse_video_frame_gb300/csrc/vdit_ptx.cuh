@@ -67,13 +67,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// `limit_ns` nanoseconds. On expiry (or when another thread of the CTA has
-// already given up, signalled through *abort) it records `site` in the
-// global status word (first writer wins), raises *abort and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *status, int site, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait (slow path, kept out of line): poll until the phase with the
+// given parity completes, for at most about `limit_ns` nanoseconds. On expiry,
+// or when another thread of the CTA has already given up (*abort), it records
+// `site` in the global status word (first writer wins), raises *abort and
+// returns false.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            int *status, int site, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -86,6 +86,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+// Single-thread bounded wait: one try_wait when the phase is already complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *status, int site, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, status, site, limit_ns);
+}
+
+// Warp-wide bounded wait with a warp-uniform result: one try_wait and one vote
+// when the phase is already complete.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               int *status, int site, uint64_t limit_ns) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const bool r = mbar_wait_slow(bar, parity, abort, status, site, limit_ns);
+    return __all_sync(0xffffffffu, r);
 }
 
 // ---------------------------------------------------------------- TMA
