@@ -47,8 +47,9 @@ constexpr int kBK = 128;              // keys per K/V tile
 constexpr int kStagesK = 2;           // K ring depth (a K tile is free once its S MMAs finish)
 constexpr int kStagesV = 3;           // V ring depth (V is held until P.V finishes)
 constexpr int kThreads = 320;
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpTma = 1;
+constexpr int kWarpMma = 0;
+constexpr int kWarpSoftmax0 = 2;      // softmax warpgroups: warps 2-5 and 6-9
 constexpr int kHalfBytes = 128 * 128; // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr float kLazyRescale = 8.0f;  // online: rescale only when the max rises > 2^8
@@ -340,7 +341,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         mma_commit(bar(kBarSfull + q));
                     }
                 }
-                __syncwarp();
             }
             for (int j = 0; j < u.nkt && ok; ++j) {
                 const uint32_t c = kc0 + j;
@@ -360,7 +360,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         issue_pv(q, sv, nmma, j > 0);
                         if (j == u.nkt - 1) mma_commit(bar(kBarOfull + q));
                     }
-                    __syncwarp();
                     ++sq[q];
                     if (j + 1 < u.nkt) {
                         if (q == 0) {
@@ -371,7 +370,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             issue_s(q, sk1, (nvalid1 + 15) & ~15);
                             mma_commit(bar(kBarSfull + q));
                         }
-                        __syncwarp();
                     }
                 }
             }
@@ -382,9 +380,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (leader) mma_commit(bar(kBarFinal));
         __syncwarp();
         drain_wait(bar(kBarFinal), 0, tlim);
-    } else if (warp < 8) {
+    } else if (warp >= kWarpSoftmax0) {
         // ------------------------------------------------------------ softmax warpgroups
-        const int q = warp / 4;                  // query tile of this warpgroup
+        const int q = (warp - kWarpSoftmax0) / 4; // query tile of this warpgroup
         const int r = threadIdx.x % kTileRows;   // row within the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
         const uint32_t tS = tmem + L::kTmemS + q * 128 + lane_off;
@@ -489,17 +487,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 {
                     uint32_t v[128];
                     tmem_ld128(tS, v);
+                    const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-mrow, -mrow);
+                    uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {      // P stored 32 packed columns at a time
                         uint32_t pk[32];
                         if (nvalid >= kBK) {
+                            // column pairs: one f32x2 FMA for the scaled, shifted logits and
+                            // one f32x2 add for the row sums
                             static_for<32>([&](auto E) {
                                 constexpr int e = decltype(E)::value;
                                 const int i0 = hf * 64 + 2 * e;
-                                const float p0 = softmax_exp2<2 * e>(fmaf(__uint_as_float(v[i0]), sc, -mrow));
-                                const float p1 = softmax_exp2<2 * e + 1>(fmaf(__uint_as_float(v[i0 + 1]), sc, -mrow));
-                                l0 += p0;
-                                l1 += p1;
+                                float x0, x1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i0]), __uint_as_float(v[i0 + 1])), sc2, nm2),
+                                          x0, x1);
+                                const float p0 = softmax_exp2<2 * e>(x0);
+                                const float p1 = softmax_exp2<2 * e + 1>(x1);
+                                l2 = f2_add(l2, f2_pack(p0, p1));
                                 pk[e] = pack_bf16(p0, p1);
                             });
                         } else {
@@ -516,6 +520,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                         tmem_st32(tS + hf * 32, pk);
                     }
+                    float a0, a1;
+                    f2_unpack(l2, a0, a1);
+                    l0 += a0;
+                    l1 += a1;
                 }
                 tmem_wait_st();
                 tc_fence_before();
