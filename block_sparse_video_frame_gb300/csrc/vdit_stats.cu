@@ -8,9 +8,10 @@
 //   c    = (1/N) sum_j k_j          R  = max_j |k_j - c|
 //   Qm   = max_i |q_i|              G  = 2 * scale * Qm * R,  eligible = G <= tau
 // HBM-bound: K is read twice (the second read mostly from L2), Q once.
-// Three launches, every reduction in a fixed order (bitwise reproducible):
-//   stats_pass1    per chunk of rows: column sums of K, max |q|^2
-//   stats_pass2    c from the chunk sums; per chunk: max |k - c|^2
+// Four launches, every reduction in a fixed order (bitwise reproducible):
+//   stats_pass1    per chunk of 512 rows: column sums of K, max |q|^2
+//   stats_mean     c = (sum of the chunk column sums) / N, per head
+//   stats_pass2    per chunk: max |k - c|^2
 //   stats_finalize R, Qm, G, eligibility
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -22,7 +23,7 @@
 namespace vdit {
 namespace {
 
-constexpr int kRowsPerChunk = 1024;
+constexpr int kRowsPerChunk = 512;
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
 
@@ -36,18 +37,18 @@ struct StatsArgs {
     uint8_t *elig;
 };
 
-template <int EPT>
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *row, int lane, float (&x)[EPT]) {
-    if constexpr (EPT == 4) {
-        uint2 u = *reinterpret_cast<const uint2 *>(row + lane * 4);
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u.x);
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u.y);
-        x[0] = __low2float(a); x[1] = __high2float(a);
-        x[2] = __low2float(b); x[3] = __high2float(b);
-    } else {
-        uint32_t u = *reinterpret_cast<const uint32_t *>(row + lane * 2);
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u);
-        x[0] = __low2float(a); x[1] = __high2float(a);
+// Each lane loads 16 bytes (8 bf16) of a row; a row of D elements takes
+// D/8 lanes, so one warp-wide load covers 32/(D/8) rows. Every warp keeps
+// kUnroll such loads per tensor in flight.
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
 }
 
@@ -61,43 +62,66 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+// sum over the LPR lanes that hold one row (a contiguous, aligned group of lanes)
+template <int LPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
-    constexpr int EPT = D / 32;
-    __shared__ float s_col[kStatsWarps][D];
+    constexpr int LPR = D / 8;          // lanes per row
+    constexpr int RPW = 32 / LPR;       // rows per warp-wide load
+    __shared__ float s_col[kStatsWarps * RPW][D];
     __shared__ float s_q[kStatsWarps];
     const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1;
-    const __nv_bfloat16 *qb = a.q + b * a.qs0 + h * a.qs1;
+    const int sub = lane / LPR, col = (lane % LPR) * 8;
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1 + col;
+    const __nv_bfloat16 *qb = a.q + b * a.qs0 + h * a.qs1 + col;
     const int r0 = chunk * kRowsPerChunk;
     const int r1 = min(a.N, r0 + kRowsPerChunk);
-    float acc[EPT];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float qm2 = 0.f;
-    for (int r = r0 + warp; r < r1; r += kStatsWarps) {
-        float x[EPT];
-        load_row<EPT>(kb + r * a.ks2, lane, x);
+    constexpr int kStep = kStatsWarps * RPW;        // rows covered by the block per load
+    // warp-uniform loop bound: every lane runs the same iterations (the row
+    // sums below shuffle across the whole warp); rows past the chunk load zeros
+    for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll) {
+        float xk[kUnroll][8], xq[kUnroll][8];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[e] += x[e];
-        load_row<EPT>(qb + r * a.qs2, lane, x);
-        float s = 0.f;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int r = wbase + sub + u * kStep;
+            if (r < r1) {
+                load8(kb + (long long)r * a.ks2, xk[u]);
+                load8(qb + (long long)r * a.qs2, xq[u]);
+            } else {
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) s = fmaf(x[e], x[e], s);
-        qm2 = fmaxf(qm2, warp_sum(s));
+                for (int e = 0; e < 8; ++e) xk[u][e] = xq[u][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += xk[u][e];
+            float sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sq = fmaf(xq[u][e], xq[u][e], sq);
+            qm2 = fmaxf(qm2, row_sum<LPR>(sq));
+        }
     }
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) s_col[warp][lane * EPT + e] = acc[e];
+    for (int e = 0; e < 8; ++e) s_col[warp * RPW + sub][col + e] = acc[e];
+    qm2 = warp_max(qm2);
     if (lane == 0) s_q[warp] = qm2;
     __syncthreads();
     const size_t slot = (size_t)bh * a.nchunk + chunk;
     for (int d = threadIdx.x; d < D; d += kStatsThreads) {
-        float s = 0.f;
+        float t = 0.f;
 #pragma unroll
-        for (int w = 0; w < kStatsWarps; ++w) s += s_col[w][d];
-        a.ws_colsum[slot * D + d] = s;
+        for (int w = 0; w < kStatsWarps * RPW; ++w) t += s_col[w][d];
+        a.ws_colsum[slot * D + d] = t;
     }
     if (threadIdx.x == 0) {
         float m = 0.f;
@@ -106,39 +130,56 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
     }
 }
 
+// c = (1/N) * sum of the chunk column sums, chunks in ascending order.
+__global__ void stats_mean(StatsArgs a, int D) {
+    const int bh = blockIdx.x;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float t = 0.f;
+        for (int c = 0; c < a.nchunk; ++c) t += a.ws_colsum[((size_t)bh * a.nchunk + c) * D + d];
+        a.k_mean[(size_t)bh * D + d] = t / (float)a.N;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
-    constexpr int EPT = D / 32;
-    __shared__ float s_c[D];
+    constexpr int LPR = D / 8;
+    constexpr int RPW = 32 / LPR;
     __shared__ float s_r[kStatsWarps];
     const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int d = threadIdx.x; d < D; d += kStatsThreads) {
-        float s = 0.f;
-        for (int c = 0; c < a.nchunk; ++c) s += a.ws_colsum[((size_t)bh * a.nchunk + c) * D + d];
-        const float mean = s / (float)a.N;
-        s_c[d] = mean;
-        if (chunk == 0) a.k_mean[(size_t)bh * D + d] = mean;
-    }
-    __syncthreads();
-    float cm[EPT];
+    const int sub = lane / LPR, col = (lane % LPR) * 8;
+    float cm[8];
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) cm[e] = s_c[lane * EPT + e];
-    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1;
+    for (int e = 0; e < 8; ++e) cm[e] = a.k_mean[(size_t)bh * D + col + e];
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1 + col;
     const int r0 = chunk * kRowsPerChunk;
     const int r1 = min(a.N, r0 + kRowsPerChunk);
+    constexpr int kStep = kStatsWarps * RPW;
     float rm2 = 0.f;
-    for (int r = r0 + warp; r < r1; r += kStatsWarps) {
-        float x[EPT];
-        load_row<EPT>(kb + r * a.ks2, lane, x);
-        float s = 0.f;
+    for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll) {
+        float xk[kUnroll][8];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-            const float t = x[e] - cm[e];
-            s = fmaf(t, t, s);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int r = wbase + sub + u * kStep;
+            if (r < r1) {
+                load8(kb + (long long)r * a.ks2, xk[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xk[u][e] = cm[e];   // contributes 0
+            }
         }
-        rm2 = fmaxf(rm2, warp_sum(s));
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float t = xk[u][e] - cm[e];
+                sq = fmaf(t, t, sq);
+            }
+            rm2 = fmaxf(rm2, row_sum<LPR>(sq));
+        }
     }
+    rm2 = warp_max(rm2);
     if (lane == 0) s_r[warp] = rm2;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -238,9 +279,11 @@ extern "C" vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, i
     dim3 grid(a.nchunk, B * H);
     if (D == 128) {
         stats_pass1<128><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
         stats_pass2<128><<<grid, kStatsThreads, 0, s>>>(a);
     } else {
         stats_pass1<64><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
         stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
     }
     stats_finalize<<<B * H, 32, 0, s>>>(a);
@@ -328,7 +371,7 @@ extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int3
     const size_t need = vdit_key_stats_workspace_size(B, H, N, D);
     if (need > kNoAllocScratchBytes) {
         set_error("vdit_key_stats_noalloc: these sizes need %zu bytes of scratch, more than the "
-                  "built-in %zu bytes (B*H*ceil(N/1024)*(D+2)*4 must not exceed it); use "
+                  "built-in %zu bytes (B*H*ceil(N/512)*(D+2)*4 must not exceed it); use "
                   "vdit_key_stats with a caller workspace", need, kNoAllocScratchBytes);
         return VDIT_ERR_INVALID;
     }
@@ -354,9 +397,11 @@ extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int3
     dim3 grid(a.nchunk, B * H);
     if (D == 128) {
         stats_pass1<128><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
         stats_pass2<128><<<grid, kStatsThreads, 0, s>>>(a);
     } else {
         stats_pass1<64><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
         stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
     }
     stats_finalize<<<B * H, 32, 0, s>>>(a);

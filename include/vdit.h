@@ -140,7 +140,7 @@ VDIT_API vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, int
  * implicit device synchronisation. Same arguments, outputs and results as
  * vdit_key_stats, without the workspace: the scratch comes from a 4 MiB array
  * compiled into the library, resident on every GPU that loads it until the
- * process exits. Sizes with B*H*ceil(N/1024)*(D+2)*4 > 4 MiB are rejected with
+ * process exits. Sizes with B*H*ceil(N/512)*(D+2)*4 > 4 MiB are rejected with
  * VDIT_ERR_INVALID before any launch. The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. All calls share the array
