@@ -50,6 +50,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the one-line contract: time the attention call on every "
+                         "workload and the dense eligibility sweep in AUTO, ONLINE and STATIC "
+                         "modes, one JSON line per (workload, mode)")
     ap.add_argument("--traffic-bytes", type=float, default=None,
                     help="dram bytes per attention launch from an ncu capture (reported as is)")
     return ap.parse_args(argv)
@@ -272,10 +276,54 @@ def config_of(w, args):
             "l2": "no flush: Q+K+V inputs are larger than the 126 MB L2"}
 
 
+def run_sweep(args):
+    """Attention-call timing per workload and softmax mode (static bound vs
+    online), with each head's eligibility: the dense base-DiT sweep reports what
+    the static-max path buys and how many heads fall back."""
+    import torch
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+    torch.cuda.set_device(0)
+    vd.load_library()
+    workloads = [configs.SR720, configs.SR1080, configs.DENSE] + configs.dense_sweep()
+    for w in workloads:
+        q, k, v = (t.cuda() for t in synth.make_qkv(w))
+        plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+        st = vd.key_stats(q, k, w.scale)
+        flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=q.device)
+        elig = st["eligible"].float().mean().item()
+        for mode in ("auto", "online", "static"):
+            for _ in range(3):
+                vd.attn_fwd(plan, q, k, v, st, w.scale, mode=mode, out=o, lse=lse)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 10
+            e0.record()
+            for _ in range(n):
+                vd.attn_fwd(plan, q, k, v, st, w.scale, mode=mode, out=o, lse=lse)
+            e1.record()
+            torch.cuda.synchronize()
+            if plan.status() != 0:
+                raise RuntimeError(f"expired wait in {w.name} {mode}")
+            ms = e0.elapsed_time(e1) / n
+            print(json.dumps({"workload": w.name, "mode": mode, "ms_per_call": ms,
+                              "tflops": flops / (ms * 1e-3) / 1e12,
+                              "eligible_fraction": elig, "fallback_heads": int(round((1 - elig) * w.B * w.H)),
+                              "key_offset_scale": w.key_offset_scale, "outlier_heads": len(w.outlier_heads),
+                              "live_pairs_per_head": plan.live_pairs}), flush=True)
+        del q, k, v, o, lse
+        plan.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist
