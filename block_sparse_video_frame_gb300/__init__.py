@@ -25,7 +25,8 @@ VDIT_OK, VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA, VDIT_ERR_NOMEM, 
 MODES = {"auto": 0, "online": 1, "static": 2}
 EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_plan_status",
             "vdit_plan_destroy", "vdit_key_stats_workspace_size", "vdit_key_stats",
-            "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc")
+            "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc",
+            "vdit_set_wait_limit_ns")
 
 
 class VditError(RuntimeError):
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_last_error.argtypes = []
         lib.vdit_version.restype = ctypes.c_char_p
         lib.vdit_version.argtypes = []
+        lib.vdit_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.vdit_set_wait_limit_ns.restype = None
         _lib = lib
         return lib
 
@@ -282,6 +285,11 @@ def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype
         _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
         _ptr(el), m, _stream(stream)))
     return out, lse
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound (ns) of every wait inside attention kernels launched afterwards; 0 = default 1 s."""
+    load_library().vdit_set_wait_limit_ns(int(ns))
 
 
 def version() -> str:

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -169,7 +170,10 @@ __device__ __forceinline__ void key_tile(const Work &u, int j, int &start, int &
     }
 }
 
-// Wait that ignores the abort flag, used only to drain in-flight copies/MMAs.
+// Wait that ignores the abort flag, used only to drain in-flight copies/MMAs
+// before exit. It always allows the default limit (not the possibly shortened
+// limit of the ordinary waits): copies and MMAs already issued must land
+// before the CTA's shared memory and TMEM are released.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
@@ -274,13 +278,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // drain: every copy this thread issued must land before the CTA exits
             for (int s = 0; s < kStagesK; ++s) {
                 const uint32_t n_k = nk / kStagesK + ((uint32_t)s < nk % kStagesK ? 1u : 0u);
-                if (n_k > 0) drain_wait(bar(kBarKfull + s), (n_k - 1) & 1, tlim);
+                if (n_k > 0) drain_wait(bar(kBarKfull + s), (n_k - 1) & 1, kDefaultTimeoutNs);
             }
             for (int s = 0; s < kStagesV; ++s) {
                 const uint32_t n_v = nv / kStagesV + ((uint32_t)s < nv % kStagesV ? 1u : 0u);
-                if (n_v > 0) drain_wait(bar(kBarVfull + s), (n_v - 1) & 1, tlim);
+                if (n_v > 0) drain_wait(bar(kBarVfull + s), (n_v - 1) & 1, kDefaultTimeoutNs);
             }
-            if (it > 0) drain_wait(bar(kBarQfull), (it - 1) & 1, tlim);
+            if (it > 0) drain_wait(bar(kBarQfull), (it - 1) & 1, kDefaultTimeoutNs);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -379,7 +383,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // drain: all issued MMAs complete before TMEM is released
         if (leader) mma_commit(bar(kBarFinal));
         __syncwarp();
-        drain_wait(bar(kBarFinal), 0, tlim);
+        drain_wait(bar(kBarFinal), 0, kDefaultTimeoutNs);
     } else if (warp >= kWarpSoftmax0) {
         // ------------------------------------------------------------ softmax warpgroups
         const int q = (warp - kWarpSoftmax0) / 4; // query tile of this warpgroup
@@ -591,6 +595,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultTimeoutNs};
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -739,7 +744,7 @@ extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const
     prm.k_mean = k_mean; prm.k_rmax = k_rmax; prm.elig = eligible;
     prm.mode = mode;
     prm.status = plan->d_status;
-    prm.timeout_ns = kDefaultTimeoutNs;
+    prm.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const int nsm = sm_count(dev);
     if (nsm <= 0) { set_error("vdit_attn_fwd: cannot query SM count"); return VDIT_ERR_CUDA; }
     const long long grid = prm.total_work < nsm ? prm.total_work : nsm;
@@ -754,4 +759,8 @@ extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const
     }
     VDIT_CUDA_TRY(cudaGetLastError());
     return VDIT_OK;
+}
+
+extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns.store(ns == 0 ? kDefaultTimeoutNs : ns, std::memory_order_relaxed);
 }

@@ -175,6 +175,16 @@ VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const v
                           const float *k_mean, const float *k_rmax, const uint8_t *eligible,
                           int32_t mode, void *stream);
 
+/* Failure-detection test hook. Every wait inside the attention kernel is
+ * bounded; when a wait expires the kernel records which wait in the plan's
+ * status word, drains its in-flight copies and MMAs, frees its tensor memory
+ * and exits early (vdit_plan_status then returns VDIT_ERR_TIMEOUT). This sets
+ * the bound for kernels launched afterwards, process-wide: ns = 0 restores the
+ * default of one second. A tiny bound makes a normal call expire on purpose,
+ * so the early-exit path can be tested without any fault. Draining always
+ * keeps the default bound. */
+VDIT_API void vdit_set_wait_limit_ns(uint64_t ns);
+
 /* Thread-local, library-owned text of the last error on this thread ("" if none). */
 VDIT_API const char *vdit_last_error(void);
 
