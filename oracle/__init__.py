@@ -79,6 +79,17 @@ def _load():
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int64,
             _i64p, _f64p, _f64p, _f64p]
         lib.vo_attention_rows.restype = None
+        lib.vo_frame_stats.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.c_int32, _i64p, _i64p, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                       ctypes.c_double, _f64p, _f64p, _f64p, _u8p]
+        lib.vo_frame_stats.restype = None
+        lib.vo_row_bounds_frames.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int32,
+                                             ctypes.c_int64, ctypes.c_int32, _i64p, _f64p,
+                                             _f64p, ctypes.c_int32, ctypes.c_double,
+                                             ctypes.c_int64, _i64p, _f64p]
+        lib.vo_row_bounds_frames.restype = None
         _lib = lib
         return lib
 
@@ -173,6 +184,39 @@ def key_stats(q, k, scale: float, tau: float):
                          _ptr(ks, _i64p), float(scale), float(tau), _ptr(c, _f64p),
                          _ptr(R, _f64p), _ptr(qmax, _f64p), _ptr(G, _f64p), _ptr(elig, _u8p))
     return dict(c=c, R=R, qmax=qmax, G=G, elig=elig)
+
+
+def frame_stats(q, k, T: int, W: int, ref: int, scale: float, tau: float):
+    """Per query frame: R_f (largest centred norm over the keys the frame sees),
+    Qmax_f, G_f and eligibility. Returns dict of [B, H, F] arrays."""
+    qa, qc, qs = _as_input(q)
+    ka, kc, ks = _as_input(k)
+    if qc != kc:
+        raise TypeError("q and k must have the same element type")
+    B, H, N, D = ka.shape
+    F = N // T
+    R = np.zeros((B, H, F))
+    qmax = np.zeros((B, H, F))
+    G = np.zeros((B, H, F))
+    elig = np.zeros((B, H, F), dtype=np.uint8)
+    _load().vo_frame_stats(qa.ctypes.data, ka.ctypes.data, kc, B, H, N, D, _ptr(qs, _i64p),
+                           _ptr(ks, _i64p), T, W, ref, float(scale), float(tau), _ptr(R, _f64p),
+                           _ptr(qmax, _f64p), _ptr(G, _f64p), _ptr(elig, _u8p))
+    return dict(R=R, qmax=qmax, G=G, elig=elig)
+
+
+def row_bounds_frames(q, c, Rf, T: int, scale: float, rows=None):
+    """m_i = scale * (q_i . c_h + |q_i| R_{h, f(i)}) with per-query-frame R."""
+    qa, qc, qs = _as_input(q)
+    B, H, N, D = qa.shape
+    rows = _rows_arg(rows, B * H, N)
+    c = np.ascontiguousarray(np.asarray(c, dtype=np.float64))
+    Rf = np.ascontiguousarray(np.asarray(Rf, dtype=np.float64))
+    m = np.zeros(len(rows))
+    _load().vo_row_bounds_frames(qa.ctypes.data, qc, H, N, D, _ptr(qs, _i64p), _ptr(c, _f64p),
+                                 _ptr(Rf, _f64p), T, float(scale), len(rows), _ptr(rows, _i64p),
+                                 _ptr(m, _f64p))
+    return m
 
 
 def _rows_arg(rows, BH, N):

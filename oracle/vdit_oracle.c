@@ -315,3 +315,84 @@ void vo_attention_rows(const void *q, const void *k, const void *v, int dtype, i
         free(qrow);
     }
 }
+
+/* Per-query-frame key statistics ("Unchaining the Softmax": the bound's
+ * guarantee holds for windowed sparse masks, where each query row sees a
+ * different slice of the keys). For query frame f of head (b, h), with c the
+ * key mean over all N keys of the head and J(f) = { j : mask(f*T, j) } the
+ * keys that frame's queries see (tested token by token through vo_mask):
+ *   R_f    = max_{j in J(f)} |k_j - c|_2
+ *   Qmax_f = max_{i in frame f} |q_i|_2
+ *   G_f    = 2 * scale * Qmax_f * R_f,  elig_f = G_f <= tau (decided in fp32)
+ * Outputs are [B*H*F]. */
+void vo_frame_stats(const void *q, const void *k, int dtype, int32_t B, int32_t H, int64_t N,
+                    int32_t D, const int64_t *qs, const int64_t *ks, int32_t T, int32_t W,
+                    int32_t ref, double scale, double tau, double *Rf, double *qmaxf, double *Gf,
+                    uint8_t *eligf)
+{
+    const int64_t F = N / T;
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        int64_t b = bh / H, h = bh % H;
+        int64_t kb = b * ks[0] + h * ks[1], qb = b * qs[0] + h * qs[1];
+        double *c = (double *)calloc((size_t)D, sizeof(double));
+        double *kn = (double *)malloc((size_t)N * sizeof(double));
+        for (int64_t j = 0; j < N; ++j)
+            for (int32_t d = 0; d < D; ++d)
+                c[d] += elem(k, kb + j * ks[2] + d, dtype);
+        for (int32_t d = 0; d < D; ++d)
+            c[d] /= (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int32_t d = 0; d < D; ++d) {
+                double x = elem(k, kb + j * ks[2] + d, dtype) - c[d];
+                acc += x * x;
+            }
+            kn[j] = sqrt(acc);
+        }
+        for (int64_t f = 0; f < F; ++f) {
+            double r = 0.0, qm = 0.0;
+            for (int64_t j = 0; j < N; ++j)
+                if (vo_mask(T, W, ref, f * T, j) && kn[j] > r)
+                    r = kn[j];
+            for (int64_t i = f * T; i < (f + 1) * T; ++i) {
+                double acc = 0.0;
+                for (int32_t d = 0; d < D; ++d) {
+                    double x = elem(q, qb + i * qs[2] + d, dtype);
+                    acc += x * x;
+                }
+                if (sqrt(acc) > qm)
+                    qm = sqrt(acc);
+            }
+            int64_t o = bh * F + f;
+            Rf[o] = r;
+            qmaxf[o] = qm;
+            Gf[o] = 2.0 * scale * qm * r;
+            eligf[o] = ((float)Gf[o] <= (float)tau) ? 1 : 0;
+        }
+        free(c);
+        free(kn);
+    }
+}
+
+/* Row bound with the per-query-frame R: m_i = scale * (q_i . c_h + |q_i| R_{f(i)}),
+ * Rf indexed [bh * F + i / T]. */
+void vo_row_bounds_frames(const void *q, int dtype, int32_t H, int64_t N, int32_t D,
+                          const int64_t *qs, const double *c, const double *Rf, int32_t T,
+                          double scale, int64_t nrows, const int64_t *rows, double *m)
+{
+    const int64_t F = N / T;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t bh = rows[r] / N, i = rows[r] % N;
+        int64_t b = bh / H, h = bh % H;
+        int64_t qo = b * qs[0] + h * qs[1] + i * qs[2];
+        double dot = 0.0, nn = 0.0;
+        for (int32_t d = 0; d < D; ++d) {
+            double x = elem(q, qo + d, dtype);
+            dot += x * c[bh * D + d];
+            nn += x * x;
+        }
+        m[r] = scale * (dot + sqrt(nn) * Rf[bh * F + i / T]);
+    }
+}
