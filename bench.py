@@ -46,6 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="sr720p")
     ap.add_argument("--mode", choices=["auto", "online", "static"], default="auto")
+    ap.add_argument("--bound", choices=["head", "frame"], default="head",
+                    help="static-bound statistics per head (vdit_key_stats) or per plan "
+                         "segment (vdit_key_stats_framed)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -272,7 +275,7 @@ def config_of(w, args):
     return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "frames": w.F,
             "tokens_per_frame": w.T, "window_radius": w.W, "ref_frame": w.ref,
             "block_size": w.block_size, "outlier_heads": len(w.outlier_heads),
-            "mode": args.mode, "key_tile": 128, "query_tiles_per_cta": 2,
+            "mode": args.mode, "bound": args.bound, "key_tile": 128, "query_tiles_per_cta": 2,
             "l2": "no flush: Q+K+V inputs are larger than the 126 MB L2"}
 
 
@@ -293,16 +296,19 @@ def run_sweep(args):
         flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=q.device)
+        stf = vd.key_stats_framed(plan, q, k, w.scale)
         elig = st["eligible"].float().mean().item()
-        for mode in ("auto", "online", "static"):
+        for mode in ("auto", "online", "static", "auto_framed"):
+            stats = stf if mode == "auto_framed" else st
+            md = "auto" if mode == "auto_framed" else mode
             for _ in range(3):
-                vd.attn_fwd(plan, q, k, v, st, w.scale, mode=mode, out=o, lse=lse)
+                vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             n = 10
             e0.record()
             for _ in range(n):
-                vd.attn_fwd(plan, q, k, v, st, w.scale, mode=mode, out=o, lse=lse)
+                vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
             e1.record()
             torch.cuda.synchronize()
             if plan.status() != 0:
@@ -310,7 +316,9 @@ def run_sweep(args):
             ms = e0.elapsed_time(e1) / n
             print(json.dumps({"workload": w.name, "mode": mode, "ms_per_call": ms,
                               "tflops": flops / (ms * 1e-3) / 1e12,
-                              "eligible_fraction": elig, "fallback_heads": int(round((1 - elig) * w.B * w.H)),
+                              "eligible_fraction": (stf["seg_eligible"].float().mean().item()
+                                                    if mode == "auto_framed" else elig),
+                              "fallback_heads": int(round((1 - elig) * w.B * w.H)),
                               "key_offset_scale": w.key_offset_scale, "outlier_heads": len(w.outlier_heads),
                               "live_pairs_per_head": plan.live_pairs}), flush=True)
         del q, k, v, o, lse
@@ -346,16 +354,27 @@ def main(argv=None):
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
     flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
-    st = vd.key_stats(q, k, w.scale)
-    wsbuf = torch.empty(max(16, vd.key_stats_workspace_bytes(w.B, w.H, w.N, w.D)),
-                        dtype=torch.uint8, device=dev)
+    framed = args.bound == "frame"
+    if framed:
+        st = vd.key_stats_framed(plan, q, k, w.scale)
+        wsbuf = torch.empty(max(16, vd.key_stats_framed_workspace_bytes(plan, w.B, w.H, w.D)),
+                            dtype=torch.uint8, device=dev)
+    else:
+        st = vd.key_stats(q, k, w.scale)
+        wsbuf = torch.empty(max(16, vd.key_stats_workspace_bytes(w.B, w.H, w.N, w.D)),
+                            dtype=torch.uint8, device=dev)
+
+    def stats(qq, kk):
+        if framed:
+            return vd.key_stats_framed(plan, qq, kk, w.scale, workspace=wsbuf, out=st)
+        return vd.key_stats(qq, kk, w.scale, workspace=wsbuf, out=st)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(ev_a=None, ev_b=None):
         plan.rebuild()
-        vd.key_stats(q, k, w.scale, workspace=wsbuf, out=st)
+        stats(q, k)
         if ev_a is not None:
             ev_a.record(stream)
         vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, out=o, lse=lse)
@@ -399,8 +418,7 @@ def main(argv=None):
         qe, ke, ve = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         for _ in range(2):
             qe.copy_(q_h, non_blocking=True); ke.copy_(k_h, non_blocking=True); ve.copy_(v_h, non_blocking=True)
-            vd.attn_fwd(plan, qe, ke, ve, vd.key_stats(qe, ke, w.scale, workspace=wsbuf, out=st),
-                        w.scale, mode=args.mode, out=o, lse=lse)
+            vd.attn_fwd(plan, qe, ke, ve, stats(qe, ke), w.scale, mode=args.mode, out=o, lse=lse)
             o_h.copy_(o, non_blocking=True)
         barrier()
         e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -409,7 +427,7 @@ def main(argv=None):
         for _ in range(ke_steps):
             qe.copy_(q_h, non_blocking=True); ke.copy_(k_h, non_blocking=True); ve.copy_(v_h, non_blocking=True)
             plan.rebuild()
-            vd.key_stats(qe, ke, w.scale, workspace=wsbuf, out=st)
+            stats(qe, ke)
             vd.attn_fwd(plan, qe, ke, ve, st, w.scale, mode=args.mode, out=o, lse=lse)
             o_h.copy_(o, non_blocking=True)
         e_b.record(stream)

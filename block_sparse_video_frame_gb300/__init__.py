@@ -26,7 +26,8 @@ MODES = {"auto": 0, "online": 1, "static": 2}
 EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_plan_status",
             "vdit_plan_destroy", "vdit_key_stats_workspace_size", "vdit_key_stats",
             "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc",
-            "vdit_set_wait_limit_ns")
+            "vdit_set_wait_limit_ns", "vdit_key_stats_framed_workspace_size",
+            "vdit_key_stats_framed", "vdit_attn_fwd_framed")
 
 
 class VditError(RuntimeError):
@@ -83,6 +84,14 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_last_error.argtypes = []
         lib.vdit_version.restype = ctypes.c_char_p
         lib.vdit_version.argtypes = []
+        lib.vdit_key_stats_framed_workspace_size.argtypes = [vp, i32, i32, i32]
+        lib.vdit_key_stats_framed_workspace_size.restype = ctypes.c_size_t
+        lib.vdit_key_stats_framed.argtypes = [vp, vp, vp, i32, i32, i32, _I64x3, _I64x3, f32, f32,
+                                              vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.vdit_key_stats_framed.restype = ctypes.c_int
+        lib.vdit_attn_fwd_framed.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, _I64x3,
+                                             _I64x3, _I64x3, _I64x3, f32, vp, vp, vp, i32, vp]
+        lib.vdit_attn_fwd_framed.restype = ctypes.c_int
         lib.vdit_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.vdit_set_wait_limit_ns.restype = None
         _lib = lib
@@ -245,6 +254,40 @@ def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None, out=None):
     return out
 
 
+def key_stats_framed(plan: Plan, q, k, scale, tau=64.0, stream=None, workspace=None, out=None):
+    """Key statistics with the bound tightened per plan segment (vdit_key_stats_framed).
+    Returns dict(k_mean [B,H,D], seg_rmax, seg_gap [B,H,nseg] fp32, seg_eligible [B,H,nseg] u8)."""
+    import torch
+    _check_bhnd("q", q)
+    _check_bhnd("k", k, q.shape[3])
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or q.shape != k.shape:
+        raise ValueError("q and k must be bf16 tensors of one shape")
+    B, H, N, D = q.shape
+    if N != plan.num_tokens:
+        raise ValueError(f"sequence length {N} != plan's num_tokens {plan.num_tokens}")
+    lib = load_library()
+    dev = q.device
+    S = int(plan.info.n_segments)
+    if out is None:
+        out = dict(k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev),
+                   seg_rmax=torch.empty((B, H, S), dtype=torch.float32, device=dev),
+                   seg_gap=torch.empty((B, H, S), dtype=torch.float32, device=dev),
+                   seg_eligible=torch.empty((B, H, S), dtype=torch.uint8, device=dev))
+    need = int(lib.vdit_key_stats_framed_workspace_size(plan.handle, B, H, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(lib.vdit_key_stats_framed(plan.handle, _ptr(q), _ptr(k), B, H, D, _strides(q), _strides(k),
+                                     float(scale), float(tau), _ptr(out["k_mean"]),
+                                     _ptr(out["seg_rmax"]), _ptr(out["seg_gap"]),
+                                     _ptr(out["seg_eligible"]), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def key_stats_framed_workspace_bytes(plan: Plan, B, H, D) -> int:
+    return int(load_library().vdit_key_stats_framed_workspace_size(plan.handle, int(B), int(H), int(D)))
+
+
 def key_stats_workspace_bytes(B, H, N, D) -> int:
     return int(load_library().vdit_key_stats_workspace_size(int(B), int(H), int(N), int(D)))
 
@@ -278,12 +321,14 @@ def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype
                                 and tuple(lse.shape) == (B, H, N)):
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
     km = kr = el = None
+    framed = stats is not None and "seg_rmax" in stats
     if stats is not None:
-        km, kr, el = stats["k_mean"], stats["k_rmax"], stats["eligible"]
-    _check(load_library().vdit_attn_fwd(
-        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), o_code, _ptr(lse), B, H, D,
-        _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
-        _ptr(el), m, _stream(stream)))
+        km = stats["k_mean"]
+        kr, el = (stats["seg_rmax"], stats["seg_eligible"]) if framed else (stats["k_rmax"], stats["eligible"])
+    fn = load_library().vdit_attn_fwd_framed if framed else load_library().vdit_attn_fwd
+    _check(fn(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), o_code, _ptr(lse), B, H, D,
+              _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
+              _ptr(el), m, _stream(stream)))
     return out, lse
 
 

@@ -40,6 +40,8 @@ def _fingerprint() -> str:
     h.update(" ".join(_flags()).encode())
     for d, names in ((CSRC, sorted(os.listdir(CSRC))), (INCLUDE, sorted(os.listdir(INCLUDE)))):
         for n in names:
+            if not n.endswith((".cu", ".cuh", ".h")) or not os.path.isfile(os.path.join(d, n)):
+                continue
             with open(os.path.join(d, n), "rb") as f:
                 h.update(n.encode())
                 h.update(f.read())

@@ -112,6 +112,9 @@ struct Params {
     float scale_log2;  // scale * log2(e)
     const float *k_mean, *k_rmax;
     const uint8_t *elig;
+    const float *seg_rmax;       // per (b, h, segment) bound and eligibility, or null
+    const uint8_t *seg_elig;
+    int nseg;
     int mode;
     int *status;
     unsigned long long timeout_ns;
@@ -121,7 +124,7 @@ struct Work {
     int b, h, bh;
     int row0, rows;        // segment rows
     int lo0, hi0, lo1, hi1;
-    int pair, ntile;       // this unit's tile pair, tiles in the segment
+    int seg, pair, ntile;  // segment, this unit's tile pair, tiles in the segment
     int nact;              // active query tiles (1 or 2)
     int nt0, nkt;          // key tiles of run 0, total key tiles
 };
@@ -144,6 +147,7 @@ __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
     const int code = p.units[ui];
     const int32_t *s = p.segments + kSegInts * (code >> 16);
     u.pair = code & 0xFFFF;
+    u.seg = code >> 16;
     u.row0 = s[0]; u.rows = s[1];
     u.lo0 = s[2]; u.hi0 = s[3]; u.lo1 = s[4]; u.hi1 = s[5];
     u.ntile = s[6];
@@ -404,8 +408,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool releaser = q == u.nact - 1 && (warp % 4) == 0 && lane == 0;
             const uint32_t kc0 = kc;
             kc += u.nkt;
-            const bool stat = p.mode == VDIT_MODE_FORCE_STATIC ||
-                              (p.mode == VDIT_MODE_AUTO && p.elig[u.bh] != 0);
+            const bool stat =
+                p.mode == VDIT_MODE_FORCE_STATIC ||
+                (p.mode == VDIT_MODE_AUTO && (p.seg_elig ? p.seg_elig[(size_t)u.bh * p.nseg + u.seg]
+                                                          : p.elig[u.bh]) != 0);
             ok = mbar_wait_warp(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
             if (!ok) break;
             // row bound ("Unchaining the Softmax"): m~ = scale*log2e*(q.c + |q| R)
@@ -433,7 +439,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     }
                 }
-                mt = sc * (dot + sqrtf(nn) * p.k_rmax[u.bh]);
+                const float R = p.seg_rmax ? p.seg_rmax[(size_t)u.bh * p.nseg + u.seg] : p.k_rmax[u.bh];
+                mt = sc * (dot + sqrtf(nn) * R);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarQfree));
@@ -664,13 +671,14 @@ int sm_count(int device) {
 
 using namespace vdit;
 
-extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k,
-                                     const void *v, void *o, int32_t o_dtype, float *lse,
-                                     int32_t B, int32_t H, int32_t D, const int64_t q_strides[3],
-                                     const int64_t k_strides[3], const int64_t v_strides[3],
-                                     const int64_t o_strides[3], float scale, const float *k_mean,
-                                     const float *k_rmax, const uint8_t *eligible, int32_t mode,
-                                     void *stream) {
+namespace {
+vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, const void *v, void *o,
+                          int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
+                          const int64_t q_strides[3], const int64_t k_strides[3],
+                          const int64_t v_strides[3], const int64_t o_strides[3], float scale,
+                          const float *k_mean, const float *k_rmax, const uint8_t *eligible,
+                          const float *seg_rmax, const uint8_t *seg_elig, int32_t mode,
+                          void *stream) {
     clear_error();
     if (!plan) { set_error("vdit_attn_fwd: plan is NULL"); return VDIT_ERR_INVALID; }
     if (!q || !k || !v || !o || !q_strides || !k_strides || !v_strides || !o_strides) {
@@ -742,6 +750,7 @@ extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const
     prm.lse = lse;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
     prm.k_mean = k_mean; prm.k_rmax = k_rmax; prm.elig = eligible;
+    prm.seg_rmax = seg_rmax; prm.seg_elig = seg_elig; prm.nseg = plan->h.n_segments;
     prm.mode = mode;
     prm.status = plan->d_status;
     prm.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -759,6 +768,44 @@ extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const
     }
     VDIT_CUDA_TRY(cudaGetLastError());
     return VDIT_OK;
+}
+
+}  // namespace
+
+extern "C" vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k,
+                                     const void *v, void *o, int32_t o_dtype, float *lse,
+                                     int32_t B, int32_t H, int32_t D, const int64_t q_strides[3],
+                                     const int64_t k_strides[3], const int64_t v_strides[3],
+                                     const int64_t o_strides[3], float scale, const float *k_mean,
+                                     const float *k_rmax, const uint8_t *eligible, int32_t mode,
+                                     void *stream) {
+    return attn_fwd_impl(plan, q, k, v, o, o_dtype, lse, B, H, D, q_strides, k_strides, v_strides,
+                         o_strides, scale, k_mean, k_rmax, eligible, nullptr, nullptr, mode, stream);
+}
+
+extern "C" vdit_status vdit_attn_fwd_framed(const vdit_plan *plan, const void *q, const void *k,
+                                            const void *v, void *o, int32_t o_dtype, float *lse,
+                                            int32_t B, int32_t H, int32_t D,
+                                            const int64_t q_strides[3], const int64_t k_strides[3],
+                                            const int64_t v_strides[3], const int64_t o_strides[3],
+                                            float scale, const float *k_mean, const float *seg_rmax,
+                                            const uint8_t *seg_eligible, int32_t mode,
+                                            void *stream) {
+    if (mode != VDIT_MODE_FORCE_ONLINE && (!k_mean || !seg_rmax)) {
+        clear_error();
+        set_error("vdit_attn_fwd_framed: k_mean and seg_rmax are required unless mode is FORCE_ONLINE");
+        return VDIT_ERR_INVALID;
+    }
+    if (mode == VDIT_MODE_AUTO && !seg_eligible) {
+        clear_error();
+        set_error("vdit_attn_fwd_framed: seg_eligible is required in AUTO mode");
+        return VDIT_ERR_INVALID;
+    }
+    // the per-head arguments are replaced by the per-segment ones; pass non-null
+    // placeholders through the shared validation, the kernel reads the segment arrays
+    return attn_fwd_impl(plan, q, k, v, o, o_dtype, lse, B, H, D, q_strides, k_strides, v_strides,
+                         o_strides, scale, k_mean, seg_rmax, seg_eligible, seg_rmax, seg_eligible,
+                         mode, stream);
 }
 
 extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {

@@ -31,6 +31,7 @@ struct StatsArgs {
     const __nv_bfloat16 *q, *k;
     long long qs0, qs1, qs2, ks0, ks1, ks2;
     int B, H, N, nchunk;
+    int T, cpf;          // rows per frame (N when frames are not used) and chunks per frame
     float scale, tau;
     float *ws_colsum, *ws_qn2, *ws_rn2;
     float *k_mean, *k_rmax, *q_nmax, *gap;
@@ -81,8 +82,9 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
     const int sub = lane / LPR, col = (lane % LPR) * 8;
     const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1 + col;
     const __nv_bfloat16 *qb = a.q + b * a.qs0 + h * a.qs1 + col;
-    const int r0 = chunk * kRowsPerChunk;
-    const int r1 = min(a.N, r0 + kRowsPerChunk);
+    const int fr = chunk / a.cpf;
+    const int r0 = fr * a.T + (chunk % a.cpf) * kRowsPerChunk;
+    const int r1 = min((fr + 1) * a.T, r0 + kRowsPerChunk);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float qm2 = 0.f;
     constexpr int kStep = kStatsWarps * RPW;        // rows covered by the block per load
@@ -152,8 +154,9 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) cm[e] = a.k_mean[(size_t)bh * D + col + e];
     const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks1 + col;
-    const int r0 = chunk * kRowsPerChunk;
-    const int r1 = min(a.N, r0 + kRowsPerChunk);
+    const int fr = chunk / a.cpf;
+    const int r0 = fr * a.T + (chunk % a.cpf) * kRowsPerChunk;
+    const int r1 = min((fr + 1) * a.T, r0 + kRowsPerChunk);
     constexpr int kStep = kStatsWarps * RPW;
     float rm2 = 0.f;
     for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll) {
@@ -209,6 +212,30 @@ __global__ void stats_finalize(StatsArgs a) {
 }
 
 int nchunks(int N) { return (N + kRowsPerChunk - 1) / kRowsPerChunk; }
+
+// Per (b, h, segment of a plan): R over the key frames the segment's queries see
+// and Qmax over the segment's query frames, from the frame-aligned chunk maxima.
+__global__ void stats_segments(StatsArgs a, const int32_t *segments, int nseg, float *seg_rmax,
+                               float *seg_gap, uint8_t *seg_elig) {
+    const int bh = blockIdx.x;
+    const float *rn2 = a.ws_rn2 + (size_t)bh * a.nchunk;
+    const float *qn2 = a.ws_qn2 + (size_t)bh * a.nchunk;
+    for (int sg = threadIdx.x; sg < nseg; sg += blockDim.x) {
+        const int32_t *g = segments + kSegInts * sg;
+        float r2 = 0.f, q2 = 0.f;
+        for (int run = 0; run < 2; ++run)
+            for (int f = g[2 + 2 * run] / a.T; f < g[3 + 2 * run] / a.T; ++f)
+                for (int c = f * a.cpf; c < (f + 1) * a.cpf; ++c) r2 = fmaxf(r2, rn2[c]);
+        for (int f = g[0] / a.T; f < (g[0] + g[1]) / a.T; ++f)
+            for (int c = f * a.cpf; c < (f + 1) * a.cpf; ++c) q2 = fmaxf(q2, qn2[c]);
+        const float R = sqrtf(r2), Qm = sqrtf(q2);
+        const float G = 2.0f * a.scale * Qm * R;
+        const size_t o = (size_t)bh * nseg + sg;
+        seg_rmax[o] = R;
+        seg_gap[o] = G;
+        seg_elig[o] = (G <= a.tau) ? 1 : 0;
+    }
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -268,6 +295,7 @@ extern "C" vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, i
     a.qs0 = q_strides[0]; a.qs1 = q_strides[1]; a.qs2 = q_strides[2];
     a.ks0 = k_strides[0]; a.ks1 = k_strides[1]; a.ks2 = k_strides[2];
     a.B = B; a.H = H; a.N = N; a.nchunk = nchunks(N);
+    a.T = N; a.cpf = a.nchunk;
     a.scale = scale; a.tau = tau;
     const size_t slots = (size_t)B * H * a.nchunk;
     a.ws_colsum = static_cast<float *>(workspace);
@@ -386,6 +414,7 @@ extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int3
     a.qs0 = q_strides[0]; a.qs1 = q_strides[1]; a.qs2 = q_strides[2];
     a.ks0 = k_strides[0]; a.ks1 = k_strides[1]; a.ks2 = k_strides[2];
     a.B = B; a.H = H; a.N = N; a.nchunk = nchunks(N);
+    a.T = N; a.cpf = a.nchunk;
     a.scale = scale; a.tau = tau;
     const size_t slots = (size_t)B * H * a.nchunk;
     a.ws_colsum = static_cast<float *>(scratch);
@@ -405,6 +434,89 @@ extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int3
         stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
     }
     stats_finalize<<<B * H, 32, 0, s>>>(a);
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
+}
+
+extern "C" size_t vdit_key_stats_framed_workspace_size(const vdit_plan *plan, int32_t B, int32_t H,
+                                                       int32_t D) {
+    if (!plan || B < 1 || H < 1 || D < 1) return 0;
+    const size_t slots = (size_t)B * H * plan->F * nchunks(plan->T);
+    return slots * (size_t)(D + 2) * sizeof(float);
+}
+
+extern "C" vdit_status vdit_key_stats_framed(const vdit_plan *plan, const void *q, const void *k,
+                                             int32_t B, int32_t H, int32_t D,
+                                             const int64_t q_strides[3], const int64_t k_strides[3],
+                                             float scale, float tau, float *k_mean, float *seg_rmax,
+                                             float *seg_gap, uint8_t *seg_eligible, void *workspace,
+                                             size_t workspace_bytes, void *stream) {
+    clear_error();
+    if (!plan || !q || !k || !q_strides || !k_strides || !k_mean || !seg_rmax || !seg_gap ||
+        !seg_eligible || !workspace) {
+        set_error("vdit_key_stats_framed: NULL pointer argument");
+        return VDIT_ERR_INVALID;
+    }
+    if (B < 1 || H < 1) {
+        set_error("vdit_key_stats_framed: B=%d H=%d must be >= 1", B, H);
+        return VDIT_ERR_INVALID;
+    }
+    if (D != 64 && D != 128) {
+        set_error("vdit_key_stats_framed: head dim D=%d not supported (64 or 128)", D);
+        return VDIT_ERR_UNSUPPORTED;
+    }
+    for (int i = 0; i < 3; ++i) {
+        if (q_strides[i] <= 0 || k_strides[i] <= 0 || q_strides[i] % 8 || k_strides[i] % 8) {
+            set_error("vdit_key_stats_framed: strides must be positive multiples of 8 elements");
+            return VDIT_ERR_INVALID;
+        }
+    }
+    if (!aligned16(q) || !aligned16(k)) {
+        set_error("vdit_key_stats_framed: q and k must be 16-byte aligned");
+        return VDIT_ERR_INVALID;
+    }
+    const size_t need = vdit_key_stats_framed_workspace_size(plan, B, H, D);
+    if (workspace_bytes < need) {
+        set_error("vdit_key_stats_framed: workspace of %zu bytes < %zu needed", workspace_bytes, need);
+        return VDIT_ERR_INVALID;
+    }
+    if (!(scale > 0.f) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats_framed: scale must be > 0 and tau >= 0");
+        return VDIT_ERR_INVALID;
+    }
+    int dev = -1;
+    VDIT_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != plan->device) {
+        set_error("vdit_key_stats_framed: plan was built on device %d, current device is %d",
+                  plan->device, dev);
+        return VDIT_ERR_INVALID;
+    }
+    StatsArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.qs0 = q_strides[0]; a.qs1 = q_strides[1]; a.qs2 = q_strides[2];
+    a.ks0 = k_strides[0]; a.ks1 = k_strides[1]; a.ks2 = k_strides[2];
+    a.B = B; a.H = H; a.N = (int)plan->N;
+    a.T = plan->T; a.cpf = nchunks(plan->T); a.nchunk = plan->F * a.cpf;
+    a.scale = scale; a.tau = tau;
+    const size_t slots = (size_t)B * H * a.nchunk;
+    a.ws_colsum = static_cast<float *>(workspace);
+    a.ws_qn2 = a.ws_colsum + slots * D;
+    a.ws_rn2 = a.ws_qn2 + slots;
+    a.k_mean = k_mean; a.k_rmax = nullptr; a.q_nmax = nullptr; a.gap = nullptr; a.elig = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    dim3 grid(a.nchunk, B * H);
+    if (D == 128) {
+        stats_pass1<128><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
+        stats_pass2<128><<<grid, kStatsThreads, 0, s>>>(a);
+    } else {
+        stats_pass1<64><<<grid, kStatsThreads, 0, s>>>(a);
+        stats_mean<<<B * H, 128, 0, s>>>(a, D);
+        stats_pass2<64><<<grid, kStatsThreads, 0, s>>>(a);
+    }
+    stats_segments<<<B * H, 64, 0, s>>>(a, plan->d_segments, plan->h.n_segments, seg_rmax, seg_gap,
+                                         seg_eligible);
     VDIT_CUDA_TRY(cudaGetLastError());
     return VDIT_OK;
 }

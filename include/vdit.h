@@ -175,6 +175,43 @@ VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const v
                           const float *k_mean, const float *k_rmax, const uint8_t *eligible,
                           int32_t mode, void *stream);
 
+/* Bytes of device workspace vdit_key_stats_framed needs for this plan and sizes. */
+VDIT_API size_t vdit_key_stats_framed_workspace_size(const vdit_plan *plan, int32_t B, int32_t H,
+                                                     int32_t D);
+
+/* Key statistics with the bound tightened per query segment ("Unchaining the
+ * Softmax": the bound's guarantee holds for windowed sparse masks, where each
+ * query row sees a different slice of the keys). For every segment s of the
+ * plan (frames sharing one key-run list; one frame for sparse windows, the
+ * whole sequence when dense):
+ *   k_mean[b,h,:]       = c, the mean of all N keys of the head    fp32 [B, H, D]
+ *   seg_rmax[b,h,s]     = max |k_j - c| over the keys s sees        fp32 [B, H, nseg]
+ *   seg_gap[b,h,s]      = 2 * scale * (max |q_i| over s's rows) * seg_rmax
+ *   seg_eligible[b,h,s] = seg_gap <= tau                           uint8 [B, H, nseg]
+ * Never looser than vdit_key_stats (equal when a segment sees every key).
+ * q, k: bf16 [B, H, N, D] device tensors, N = the plan's num_tokens. workspace:
+ * at least vdit_key_stats_framed_workspace_size bytes of caller-owned device
+ * memory. Fixed-order reductions (bitwise reproducible). Errors:
+ * VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_key_stats_framed(const vdit_plan *plan, const void *q, const void *k,
+                                           int32_t B, int32_t H, int32_t D,
+                                           const int64_t q_strides[3], const int64_t k_strides[3],
+                                           float scale, float tau, float *k_mean, float *seg_rmax,
+                                           float *seg_gap, uint8_t *seg_eligible, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+
+/* vdit_attn_fwd with the per-segment bound and eligibility of
+ * vdit_key_stats_framed (same plan) in place of the per-head ones: each work
+ * unit reads R and eligibility of its own segment. Same outputs, layout,
+ * determinism and errors as vdit_attn_fwd. */
+VDIT_API vdit_status vdit_attn_fwd_framed(const vdit_plan *plan, const void *q, const void *k,
+                                          const void *v, void *o, int32_t o_dtype, float *lse,
+                                          int32_t B, int32_t H, int32_t D,
+                                          const int64_t q_strides[3], const int64_t k_strides[3],
+                                          const int64_t v_strides[3], const int64_t o_strides[3],
+                                          float scale, const float *k_mean, const float *seg_rmax,
+                                          const uint8_t *seg_eligible, int32_t mode, void *stream);
+
 /* Failure-detection test hook. Every wait inside the attention kernel is
  * bounded; when a wait expires the kernel records which wait in the plan's
  * status word, drains its in-flight copies and MMAs, frees its tensor memory
