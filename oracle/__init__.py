@@ -90,6 +90,12 @@ def _load():
                                              _f64p, ctypes.c_int32, ctypes.c_double,
                                              ctypes.c_int64, _i64p, _f64p]
         lib.vo_row_bounds_frames.restype = None
+        lib.vo_qkv_prologue.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _i64p,
+                                        _f64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                        ctypes.c_double, ctypes.c_int64, _i64p, _f64p, _f64p,
+                                        _f64p]
+        lib.vo_qkv_prologue.restype = None
         _lib = lib
         return lib
 
@@ -217,6 +223,52 @@ def row_bounds_frames(q, c, Rf, T: int, scale: float, rows=None):
                                  _ptr(Rf, _f64p), T, float(scale), len(rows), _ptr(rows, _i64p),
                                  _ptr(m, _f64p))
     return m
+
+
+def _as_matrix(x, ndim):
+    """bf16 torch / uint16 numpy (bf16 bits) / float64 -> (array, dtype code)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            if x.dtype == torch.bfloat16:
+                x = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+            elif x.dtype == torch.float64:
+                x = x.contiguous().numpy()
+            else:
+                raise TypeError(f"oracle input must be bf16 or float64, got {x.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(np.asarray(x))
+    if x.ndim != ndim:
+        raise ValueError(f"expected {ndim} dimensions, got {x.ndim}")
+    if x.dtype == np.uint16:
+        return x, 0
+    if x.dtype == np.float64:
+        return x, 1
+    raise TypeError(f"oracle input must be bf16 bits or float64, got {x.dtype}")
+
+
+def qkv_prologue(x, w, gamma, H: int, D: int, eps: float, base: float, rows=None):
+    """RMSNorm -> QKV projection -> rotary embedding on q, k (pairs i, i + D/2,
+    position = token index) -> per-head outputs. x: [B, N, C]; w: [3*H*D, C]
+    (q rows, then k, then v, head-major); gamma: [C]. Returns (q, k, v), each
+    [nrows, H, D] float64, for flattened rows b*N + n (all rows by default)."""
+    xa, xc = _as_matrix(x, 3)
+    wa, wc = _as_matrix(w, 2)
+    if xc != wc:
+        raise TypeError("x and w must have the same element type")
+    B, N, C = xa.shape
+    if wa.shape != (3 * H * D, C):
+        raise ValueError(f"w must be [{3 * H * D}, {C}], got {wa.shape}")
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float64))
+    rows = np.ascontiguousarray(np.arange(B * N, dtype=np.int64) if rows is None
+                                else np.asarray(rows, dtype=np.int64))
+    xs = np.array([N * C, C], dtype=np.int64)
+    out = [np.zeros((len(rows), H, D)) for _ in range(3)]
+    _load().vo_qkv_prologue(xa.ctypes.data, wa.ctypes.data, xc, B, N, C, _ptr(xs, _i64p),
+                            _ptr(g, _f64p), H, D, float(eps), float(base), len(rows),
+                            _ptr(rows, _i64p), *[_ptr(o, _f64p) for o in out])
+    return tuple(out)
 
 
 def _rows_arg(rows, BH, N):

@@ -396,3 +396,67 @@ void vo_row_bounds_frames(const void *q, int dtype, int32_t H, int64_t N, int32_
         m[r] = scale * (dot + sqrt(nn) * Rf[bh * F + i / T]);
     }
 }
+
+/* Fused pre-attention chain ("Layout Is the ABI", Fig. 5: normalisation,
+ * projections, rotary embeddings and head packing, written straight into the
+ * layout attention reads). For each listed token row (b, n) of x [B, N, C]:
+ *   y_c   = x_c * gamma_c / sqrt(mean_c x_c^2 + eps)                  (RMSNorm)
+ *   z_o   = sum_c y_c * w[o, c],  o in [0, 3*H*D)                      (QKV projection,
+ *           w is [3*H*D, C]: rows 0..HD-1 give q, then k, then v, head-major)
+ *   rotary embedding on q and k of every head, position n, pairs (i, i + D/2):
+ *           t_i = base^(-2i/D), a = n * t_i,
+ *           (u, w) -> (u cos a - w sin a, u sin a + w cos a)
+ * Outputs are [nrows, H, D] each (q, k, v). x and w element type: 0 = bf16, 1 = f64.
+ * x strides (elements) for (b, n); the channel dimension is contiguous.
+ * rows[r] = b * N + n. */
+void vo_qkv_prologue(const void *x, const void *w, int dtype, int32_t B, int64_t N, int32_t C,
+                     const int64_t *xs, const double *gamma, int32_t H, int32_t D, double eps,
+                     double base, int64_t nrows, const int64_t *rows, double *q_out,
+                     double *k_out, double *v_out)
+{
+    const int64_t HD = (int64_t)H * D;
+    (void)B;
+#pragma omp parallel
+    {
+        double *y = (double *)malloc((size_t)C * sizeof(double));
+        double *z = (double *)malloc((size_t)(3 * HD) * sizeof(double));
+#pragma omp for schedule(dynamic)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t b = rows[r] / N, n = rows[r] % N;
+            const int64_t xo = b * xs[0] + n * xs[1];
+            double ss = 0.0;
+            for (int32_t c = 0; c < C; ++c) {
+                double v = elem(x, xo + c, dtype);
+                ss += v * v;
+            }
+            const double inv = 1.0 / sqrt(ss / (double)C + eps);
+            for (int32_t c = 0; c < C; ++c)
+                y[c] = elem(x, xo + c, dtype) * inv * gamma[c];
+            for (int64_t o = 0; o < 3 * HD; ++o) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < C; ++c)
+                    acc += y[c] * elem(w, o * C + c, dtype);
+                z[o] = acc;
+            }
+            for (int part = 0; part < 2; ++part) {           /* q, k: rotary embedding */
+                for (int32_t h = 0; h < H; ++h) {
+                    double *zh = z + part * HD + (int64_t)h * D;
+                    for (int32_t i = 0; i < D / 2; ++i) {
+                        const double t = pow(base, -2.0 * i / (double)D);
+                        const double a = (double)n * t;
+                        const double u = zh[i], wv = zh[i + D / 2];
+                        zh[i] = u * cos(a) - wv * sin(a);
+                        zh[i + D / 2] = u * sin(a) + wv * cos(a);
+                    }
+                }
+            }
+            for (int64_t o = 0; o < HD; ++o) {
+                q_out[r * HD + o] = z[o];
+                k_out[r * HD + o] = z[HD + o];
+                v_out[r * HD + o] = z[2 * HD + o];
+            }
+        }
+        free(y);
+        free(z);
+    }
+}
