@@ -6,6 +6,8 @@ The library must be built first (``__graft_entry__.build()`` or
 ``python -m block_sparse_video_frame_gb300._build``). If it is missing, every
 call raises: there is no CPU or eager fallback.
 
+    wf = fold_gamma(w, gamma); cs = rope_table(N, D)    # "Layout Is the ABI", Fig. 5
+    q, k, v = qkv_prologue(x, wf, cs, H, D)               # RMSNorm + QKV + RoPE -> [B, H, N, D]
     plan = attn_plan(F, T, W, ref, block_size)          # "Deleting the Mask", Fig. 3
     st = key_stats(q, k, scale)                          # "Unchaining the Softmax"
     o, lse = attn_fwd(plan, q, k, v, st, scale)          # fused tcgen05 kernel
@@ -27,7 +29,8 @@ EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_p
             "vdit_plan_destroy", "vdit_key_stats_workspace_size", "vdit_key_stats",
             "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc",
             "vdit_set_wait_limit_ns", "vdit_key_stats_framed_workspace_size",
-            "vdit_key_stats_framed", "vdit_attn_fwd_framed")
+            "vdit_key_stats_framed", "vdit_attn_fwd_framed", "vdit_qkv_fold_gamma",
+            "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status")
 
 
 class VditError(RuntimeError):
@@ -94,6 +97,16 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_attn_fwd_framed.restype = ctypes.c_int
         lib.vdit_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.vdit_set_wait_limit_ns.restype = None
+        _I64x2 = ctypes.c_int64 * 2
+        lib.vdit_qkv_fold_gamma.argtypes = [vp, vp, vp, i64, i32, vp]
+        lib.vdit_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
+        lib.vdit_qkv_workspace_size.argtypes = [i32, i32]
+        lib.vdit_qkv_workspace_size.restype = ctypes.c_size_t
+        lib.vdit_qkv_prologue.argtypes = [vp, _I64x2, vp, vp, vp, vp, vp, _I64x3, _I64x3, _I64x3,
+                                          i32, i32, i32, i32, i32, f32, vp, ctypes.c_size_t, vp]
+        lib.vdit_qkv_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        for fn in ("vdit_qkv_fold_gamma", "vdit_rope_table", "vdit_qkv_prologue", "vdit_qkv_status"):
+            getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -330,6 +343,73 @@ def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype
               _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
               _ptr(el), m, _stream(stream)))
     return out, lse
+
+
+def fold_gamma(w, gamma, out=None, stream=None):
+    """W' = bf16(W * gamma) per input channel, once per weight set ("Layout Is
+    the ABI": the RMSNorm gain folded into the projection). w: bf16 [rows, C]
+    contiguous CUDA tensor; gamma: [C] (any float dtype, read as fp32)."""
+    import torch
+    if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("w must be a contiguous bf16 CUDA tensor [rows, C]")
+    g = gamma.to(device=w.device, dtype=torch.float32).contiguous()
+    if g.numel() != w.shape[1]:
+        raise ValueError("gamma must have C entries")
+    if out is None:
+        out = torch.empty_like(w)
+    _check(load_library().vdit_qkv_fold_gamma(_ptr(w), _ptr(g), _ptr(out), w.shape[0], w.shape[1],
+                                              _stream(stream)))
+    return out
+
+
+def rope_table(N, D, base=10000.0, device=None, stream=None):
+    """fp32 [D/2, N, 2] table of (cos, sin) of n * base^(-2i/D), built on the GPU in fp64."""
+    import torch
+    t = torch.empty((D // 2, N, 2), dtype=torch.float32, device=device or "cuda")
+    _check(load_library().vdit_rope_table(_ptr(t), int(N), int(D), float(base), _stream(stream)))
+    return t
+
+
+def qkv_workspace_bytes(B, N) -> int:
+    return int(load_library().vdit_qkv_workspace_size(int(B), int(N)))
+
+
+def qkv_prologue(x, w_folded, rope, H, D, eps=1e-6, out=None, workspace=None, stream=None):
+    """Fused RMSNorm -> q/k/v projection -> rotary embedding -> [B, H, N, D] bf16.
+    x: bf16 [B, N, C] CUDA tensor with a contiguous last dimension; w_folded:
+    bf16 [3HD, C] from fold_gamma; rope: fp32 [D/2, N, 2] from rope_table (or
+    any angle table in that layout). Returns (q, k, v)."""
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 3 or not x.is_cuda or x.stride(2) != 1:
+        raise ValueError("x must be a bf16 CUDA tensor [B, N, C] with a contiguous last dimension")
+    B, N, C = x.shape
+    if w_folded.shape != (3 * H * D, C) or not w_folded.is_contiguous():
+        raise ValueError(f"w_folded must be contiguous [{3 * H * D}, {C}]")
+    if rope.shape != (D // 2, N, 2) or rope.dtype != torch.float32 or not rope.is_contiguous():
+        raise ValueError(f"rope must be a contiguous fp32 [{D // 2}, {N}, 2] table")
+    if out is None:
+        out = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=x.device) for _ in range(3))
+    for name, t in zip("qkv", out):
+        _check_bhnd(name, t, D)
+    need = qkv_workspace_bytes(B, N)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    elif workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    xs = (ctypes.c_int64 * 2)(int(x.stride(0)), int(x.stride(1)))
+    q, k, v = out
+    _check(load_library().vdit_qkv_prologue(
+        _ptr(x), xs, _ptr(w_folded), _ptr(rope), _ptr(q), _ptr(k), _ptr(v), _strides(q),
+        _strides(k), _strides(v), B, N, C, int(H), int(D), float(eps), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return q, k, v
+
+
+def qkv_status(workspace, stream=None) -> int:
+    """Synchronise, return and clear the status word of a prologue workspace (0 = no expired wait)."""
+    code = ctypes.c_int32(0)
+    load_library().vdit_qkv_status(_ptr(workspace), _stream(stream), ctypes.byref(code))
+    return code.value
 
 
 def set_wait_limit_ns(ns: int) -> None:

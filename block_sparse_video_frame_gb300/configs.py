@@ -75,3 +75,35 @@ def dense_sweep():
             out.append(DENSE.with_(name=f"dense_s{s:g}_out{n_out}", key_offset_scale=s,
                                    outlier_heads=heads))
     return out
+
+
+@dataclass(frozen=True)
+class PrologueShape:
+    """Sizes of the fused pre-attention chain ("Layout Is the ABI"): B x N
+    token rows of hidden size C projected to H heads of size D for q, k, v."""
+    name: str
+    B: int
+    N: int
+    C: int
+    H: int
+    D: int
+    eps: float = 1e-6
+    base: float = 10000.0
+    seed: int = 0
+
+    @property
+    def O(self) -> int:
+        return 3 * self.H * self.D
+
+    @property
+    def flops(self) -> int:
+        """Dense projection FLOPs (2 per multiply-add)."""
+        return 2 * self.B * self.N * self.C * self.O
+
+
+# Hidden size = H * D (the attention width of the shapes above).
+PRO_TINY = PrologueShape("pro_tiny", B=1, N=200, C=128, H=2, D=64)           # ragged rows, one column tile
+PRO_RAGGED = PrologueShape("pro_ragged", B=2, N=300, C=200, H=3, D=128, seed=1)  # K tail, half column tile
+PRO_SMALL = PrologueShape("pro_small", B=1, N=3600, C=1024, H=8, D=128, seed=2)
+PRO_SR720 = PrologueShape("pro_sr720p", B=1, N=46800, C=3072, H=24, D=128, seed=3)
+PROLOGUE = (PRO_TINY, PRO_RAGGED, PRO_SMALL, PRO_SR720)

@@ -1,4 +1,5 @@
 // Error reporting and version of libvdit.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 
@@ -8,7 +9,10 @@ namespace vdit {
 
 namespace {
 thread_local char g_err[512] = "";
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 }
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -27,5 +31,9 @@ vdit_status cuda_fail(cudaError_t e, const char *what) {
 }  // namespace vdit
 
 extern "C" const char *vdit_last_error(void) { return vdit::g_err; }
+
+extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {
+    vdit::g_wait_limit_ns.store(ns == 0 ? vdit::kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+}
 
 extern "C" const char *vdit_version(void) { return "libvdit 0.1 (sm_103a, tcgen05)"; }

@@ -32,7 +32,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -602,7 +601,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
-std::atomic<unsigned long long> g_wait_limit_ns{kDefaultTimeoutNs};
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -753,7 +751,7 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
     prm.seg_rmax = seg_rmax; prm.seg_elig = seg_elig; prm.nseg = plan->h.n_segments;
     prm.mode = mode;
     prm.status = plan->d_status;
-    prm.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    prm.timeout_ns = wait_limit_ns();
     const int nsm = sm_count(dev);
     if (nsm <= 0) { set_error("vdit_attn_fwd: cannot query SM count"); return VDIT_ERR_CUDA; }
     const long long grid = prm.total_work < nsm ? prm.total_work : nsm;
@@ -806,8 +804,4 @@ extern "C" vdit_status vdit_attn_fwd_framed(const vdit_plan *plan, const void *q
     return attn_fwd_impl(plan, q, k, v, o, o_dtype, lse, B, H, D, q_strides, k_strides, v_strides,
                          o_strides, scale, k_mean, seg_rmax, seg_eligible, seg_rmax, seg_eligible,
                          mode, stream);
-}
-
-extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {
-    g_wait_limit_ns.store(ns == 0 ? kDefaultTimeoutNs : ns, std::memory_order_relaxed);
 }

@@ -24,6 +24,11 @@ vdit_status cuda_fail(cudaError_t e, const char *what);
         if (e__ != cudaSuccess) return ::vdit::cuda_fail(e__, #expr); \
     } while (0)
 
+// Bound on every spin-wait inside a kernel, set by vdit_set_wait_limit_ns
+// (default one second); draining after an expired wait always uses the default.
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+unsigned long long wait_limit_ns();
+
 // Query-tile geometry shared by the plan and the attention kernel.
 constexpr int kTileRows = 128;   // rows of one query tile (tcgen05 M)
 constexpr int kTilesPerUnit = 2; // query tiles that share one K/V stream

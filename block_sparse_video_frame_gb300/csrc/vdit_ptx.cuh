@@ -75,7 +75,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // or when another thread of the CTA has already given up (*abort), it records
 // `site` in the global status word (first writer wins), raises *abort and
 // returns false.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
                                             int *status, int site, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {

@@ -12,8 +12,17 @@ Recipe (one ``torch.Generator`` seeded per workload, draws in this order):
      j ~ U{0..N-1}; that key row (Z + mu) is multiplied by 20
   K = Z + mu; Q, K, V are rounded to bf16 (round to nearest even).
 
-The pages' production activations are not available; these draws stand in for
-them with the shapes and structure the workload presets name.
+Pre-attention chain inputs (``make_prologue_inputs``, one generator seeded
+per call, draws in this order):
+  1. x     = N(0, 1) of shape [B, N, C]          (hidden states)
+  2. w     = N(0, 1) / sqrt(C) of shape [3HD, C] (q, k, v projection rows)
+  3. gamma = 1 + 0.1 N(0, 1) of shape [C]        (RMSNorm gain, fp32)
+     or, with ``exact_gain``, 2^e with e ~ U{-1, 0, 1}, so that w * gamma is
+     exactly representable in bf16
+  x and w are rounded to bf16.
+
+The pages' production activations and weights are not available; these draws
+stand in for them with the shapes and structure the workload presets name.
 """
 from __future__ import annotations
 
@@ -40,6 +49,20 @@ def make_qkv(w: Workload, seed: int | None = None, dtype=torch.bfloat16):
             k[b, h, j, :] *= OUTLIER_FACTOR
     k = k.to(dtype)
     return q, k, v
+
+
+def make_prologue_inputs(B: int, N: int, C: int, H: int, D: int, seed: int = 0,
+                         exact_gain: bool = False):
+    """Return (x bf16 [B, N, C], w bf16 [3HD, C], gamma fp32 [C]) CPU tensors."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn((B, N, C), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    w = (torch.randn((3 * H * D, C), generator=g, dtype=torch.float32) * C ** -0.5).to(torch.bfloat16)
+    if exact_gain:
+        gamma = torch.pow(2.0, torch.randint(-1, 2, (C,), generator=g).to(torch.float32))
+    else:
+        gamma = 1.0 + 0.1 * torch.randn((C,), generator=g, dtype=torch.float32)
+    return x, w, gamma
 
 
 def bf16_bits(t: torch.Tensor):

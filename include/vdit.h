@@ -212,10 +212,85 @@ VDIT_API vdit_status vdit_attn_fwd_framed(const vdit_plan *plan, const void *q, 
                                           float scale, const float *k_mean, const float *seg_rmax,
                                           const uint8_t *seg_eligible, int32_t mode, void *stream);
 
-/* Failure-detection test hook. Every wait inside the attention kernel is
- * bounded; when a wait expires the kernel records which wait in the plan's
- * status word, drains its in-flight copies and MMAs, frees its tensor memory
- * and exits early (vdit_plan_status then returns VDIT_ERR_TIMEOUT). This sets
+/* ---------------------------------------------------------------------------
+ * Fused pre-attention chain ("Layout Is the ABI", Fig. 5). Attention's inputs
+ * come out of a chain of small steps -- normalisation, projections, rotary
+ * embeddings, head packing -- and the pages fuse that chain into one kernel
+ * that writes its result directly in the layout the next consumer reads, so
+ * no repack copies sit in between. Here the consumer is vdit_attn_fwd and the
+ * layout is [B, H, N, D]. For a token row x (length C) at position n:
+ *   y     = x / sqrt(mean_c x_c^2 + eps) * gamma                  (RMSNorm)
+ *   z     = W y,  W = [Wq; Wk; Wv] of shape [3*H*D, C], rows head-major
+ *   v_h   = z[2HD + hD + d]
+ *   q_h, k_h = z[hD + d], z[HD + hD + d], each rotated pairwise:
+ *           (u_i, u_{i+D/2}) -> (u_i cos a - u_{i+D/2} sin a, u_i sin a + u_{i+D/2} cos a)
+ *           with a = theta[n, i], i < D/2.
+ * The pages name the steps but not their variants; the readings taken are
+ * RMSNorm with a learned per-channel gain on the hidden state, one fused
+ * q/k/v projection without bias, and rotate-half rotary embedding of q and k
+ * with a caller-supplied angle table (vdit_rope_table builds the 1-D one,
+ * theta[n, i] = n * base^(-2i/D)).
+ *
+ * GPU mapping: the gain folds into the weights once (vdit_qkv_fold_gamma);
+ * per call, a pre-pass computes 1/rms of every row and one persistent tcgen05
+ * GEMM computes x W'^T with the 1/rms scale, the rotation, the bf16 rounding
+ * and the head scatter in its epilogue (TMA stores into q, k, v).
+ * ------------------------------------------------------------------------- */
+
+/* w_folded[o, c] = bf16(fp32(w[o, c]) * gamma[c]), rounded to nearest-even
+ * (the fp32 product is itself rounded to nearest). w, w_folded: bf16 [rows, C]
+ * dense device arrays (may alias); gamma: fp32 [C] device array. Done once per
+ * weight set. Errors: VDIT_ERR_INVALID (null pointer, rows < 1, C < 1),
+ * VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_qkv_fold_gamma(const void *w, const float *gamma, void *w_folded,
+                                         int64_t rows, int32_t C, void *stream);
+
+/* Rotary angle table for positions n in [0, N) and pairs i in [0, D/2):
+ *   table[(i * N + n) * 2 + 0] = cos(n * base^(-2i/D)),
+ *   table[(i * N + n) * 2 + 1] = sin(n * base^(-2i/D)),
+ * evaluated in fp64 and rounded to fp32 (layout [D/2][N][2], pair-major so
+ * that consecutive rows read consecutive entries). Any other angle schedule
+ * (e.g. per-axis angles for frame, height and width) may be written into the
+ * same layout by the caller. Errors: VDIT_ERR_INVALID (null table, N < 1,
+ * D odd or < 2, base <= 0), VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_rope_table(float *table, int32_t N, int32_t D, double base, void *stream);
+
+/* Bytes of device workspace vdit_qkv_prologue needs: one status word and one
+ * fp32 per token row. */
+VDIT_API size_t vdit_qkv_workspace_size(int32_t B, int32_t N);
+
+/* The fused chain above for every row of x.
+ *   x:        bf16, element (b, n, c) at x[b*x_strides[0] + n*x_strides[1] + c]
+ *   w_folded: bf16 [3*H*D, C] dense, the output of vdit_qkv_fold_gamma
+ *   rope:     fp32 [D/2][N][2] angle table (see vdit_rope_table)
+ *   q, k, v:  bf16 [B, H, N, D] outputs, strides in elements for (b, h, n)
+ *   eps:      RMSNorm epsilon (>= 0)
+ *   workspace: >= vdit_qkv_workspace_size(B, N) bytes of device memory; its
+ *             status word must be zero at launch (it is after a fresh cudaMemset
+ *             and after vdit_qkv_status).
+ * Requirements: D in {64, 128}; C a multiple of 8; x strides, q/k/v strides
+ * positive multiples of 8 elements; every base address 16-byte aligned.
+ * Accumulation is fp32 over bf16 products; outputs are rounded once to bf16.
+ * Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED (D), VDIT_ERR_CUDA; an expired
+ * wait inside the GEMM is reported by vdit_qkv_status. */
+VDIT_API vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[2],
+                                       const void *w_folded, const float *rope, void *q, void *k,
+                                       void *v, const int64_t q_strides[3],
+                                       const int64_t k_strides[3], const int64_t v_strides[3],
+                                       int32_t B, int32_t N, int32_t C, int32_t H, int32_t D,
+                                       float eps, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/* Synchronise `stream`, then report and clear the status word in a prologue
+ * workspace. *code receives the raw word (0 = none). Returns VDIT_OK when the
+ * word was 0, VDIT_ERR_TIMEOUT otherwise. */
+VDIT_API vdit_status vdit_qkv_status(void *workspace, void *stream, int32_t *code);
+
+/* Failure-detection test hook. Every wait inside the attention kernel and the
+ * prologue GEMM is bounded; when a wait expires the kernel records which wait
+ * in its status word (the plan's, or the prologue workspace's), drains its
+ * in-flight copies and MMAs, frees its tensor memory and exits early
+ * (vdit_plan_status / vdit_qkv_status then return VDIT_ERR_TIMEOUT). This sets
  * the bound for kernels launched afterwards, process-wide: ns = 0 restores the
  * default of one second. A tiny bound makes a normal call expire on purpose,
  * so the early-exit path can be tested without any fault. Draining always
