@@ -53,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--prologue", action="store_true",
+                    help="time the fused pre-attention chain (RMSNorm + QKV projection + rotary "
+                         "embedding + [B,H,N,D] packing) per prologue shape; one JSON line each")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the one-line contract: time the attention call on every "
                          "workload and the dense eligibility sweep in AUTO, ONLINE and STATIC "
@@ -326,12 +329,68 @@ def run_sweep(args):
     return 0
 
 
+def run_prologue(args):
+    """The fused pre-attention chain ("Layout Is the ABI") per shape: ms per
+    vdit_qkv_prologue call (1/rms pre-pass + tcgen05 GEMM with the RMSNorm,
+    rotary and packing epilogue), TFLOP/s of the dense projection, and the
+    fraction of the measured bf16 GEMM peak. Inputs: synthetic x ~ N(0, 1),
+    w ~ N(0, 1/C), gains 1 + 0.1 N(0, 1); x + w + outputs exceed L2 at the
+    720p shape, and a 256 MB buffer is rewritten between timed calls."""
+    import torch
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+    torch.cuda.set_device(0)
+    vd.load_library()
+    peaks = load_peaks()
+    peak_src = "of measured" if peaks["source"] == "measured" else "of fallback"
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for s in (configs.PRO_SMALL, configs.PRO_SR720):
+        x, w, gamma = synth.make_prologue_inputs(s.B, s.N, s.C, s.H, s.D, s.seed)
+        x, w = x.cuda(), w.cuda()
+        wf = vd.fold_gamma(w, gamma.cuda())
+        cs = vd.rope_table(s.N, s.D, s.base)
+        ws = torch.zeros(vd.qkv_workspace_bytes(s.B, s.N), dtype=torch.uint8, device="cuda")
+        out = tuple(torch.empty((s.B, s.H, s.N, s.D), dtype=torch.bfloat16, device="cuda")
+                    for _ in range(3))
+        for _ in range(max(3, args.warmup)):
+            vd.qkv_prologue(x, wf, cs, s.H, s.D, s.eps, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        times = []
+        stream = torch.cuda.current_stream()
+        for _ in range(max(5, min(args.steps, 50))):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            vd.qkv_prologue(x, wf, cs, s.H, s.D, s.eps, out=out, workspace=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        if vd.qkv_status(ws) != 0:
+            raise RuntimeError(f"expired wait in the prologue at {s.name}")
+        ms = statistics.median(times)
+        tflops = s.flops / (ms * 1e-3) / 1e12
+        print(json.dumps({
+            "workload": s.name, "metric": "dense projection TFLOP/s (RMSNorm, rotary and packing fused)",
+            "ms_per_call": ms, "tflops": tflops,
+            "config": {"B": s.B, "N": s.N, "C": s.C, "H": s.H, "D": s.D, "out_cols": s.O,
+                       "tile": "CTA pair 256x256x64 (cta_group::2), 6 stages, persistent",
+                       "l2": "256 MB buffer rewritten between timed calls"},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                         "peak_source": peak_src},
+            "launches_per_call": 2}), flush=True)
+        del x, w, wf, cs, ws, out
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.prologue:
+        return run_prologue(args)
 
     import torch
     import torch.distributed as dist

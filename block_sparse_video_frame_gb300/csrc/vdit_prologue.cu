@@ -12,20 +12,25 @@
 // so the gain folds into the weights once (fold_gamma_kernel) and each call
 // runs:
 //   rms_kernel   one warp per token row: 1/rms in fp32 (HBM-bound pre-pass)
-//   qkv_gemm     persistent tcgen05 GEMM, x [rows, C] . W'^T [C, 3HD], one CTA
-//                per SM, 128 x 256 output tiles, 64-deep K stages:
-//     warp 0     TMEM allocator and single-thread MMA issuer; two 256-column
-//                fp32 accumulators in TMEM (512 columns) so one tile's
-//                epilogue overlaps the next tile's MMAs
-//     warp 1     TMA producer: 4-stage ring of x (128 x 64) and W' (256 x 64)
-//                tiles, bf16, 128-byte swizzle
-//     warps 2-5  epilogue: thread = output row (TMEM lane); 1/rms scale,
-//                rotation of q and k heads by the angle table, bf16 rounding,
-//                128-byte-swizzled staging in shared memory, TMA stores into
-//                q, k, v ([B, H, N, D]); rows past N are clipped by the store
+//   qkv_gemm     persistent tcgen05 GEMM, x [rows, C] . W'^T [C, 3HD], on CTA
+//                pairs (clusters of 2, one CTA per SM): a pair computes a
+//                256 x 256 output tile with cta_group::2 MMAs (M = 256 over
+//                both SMs, N = 256), each CTA staging its own 128 x rows and
+//                half of the 256 W' rows, so per SM only 32 KB cross from L2
+//                per 64-deep K stage (48 KB for a lone 128 x 256 tile)
+//     warp 0     TMEM allocator (both CTAs); on rank 0 the single-thread MMA
+//                issuer. Two 256-column fp32 accumulators per CTA (512 TMEM
+//                columns) so one tile's epilogue overlaps the next tile's MMAs
+//     warp 1     TMA producer: 6-stage ring of x (128 x 64) and W' (128 x 64)
+//                tiles, bf16, 128-byte swizzle; both CTAs' loads complete on
+//                rank 0's stage barrier, where the MMA issuer waits
+//     warps 2-5  epilogue: thread = output row (TMEM lane of its CTA); 1/rms
+//                scale, rotation of q and k heads by the angle table, bf16
+//                rounding, 128-byte-swizzled staging in shared memory, TMA
+//                stores into q, k, v ([B, H, N, D]); rows past N are clipped
 // Every wait is bounded in time; on expiry the CTA records a site code in the
-// workspace status word, drains its in-flight copies and MMAs, frees TMEM and
-// exits.
+// workspace status word, both CTAs drain their in-flight copies and MMAs, free
+// TMEM and exit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,6 +62,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// Loads whose completion is signalled on an mbarrier of either CTA of the pair
+// (cluster address), for the CTA-pair MMA.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 // 4-D tiled TMA store of one box from shared memory (bulk-group completion).
@@ -104,6 +127,64 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pair (cluster of 2)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// 32-bit store to another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Count `bytes` as arrived on a local mbarrier's current phase without a copy.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// tcgen05 over the CTA pair: allocation (one warp in each CTA), MMA issued by
+// one thread of the even CTA, commits that arrive at the same barrier offset
+// in both CTAs.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma2_commit_both(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
 // Bounded waits. The GEMM's waits are short (one K stage, one tile), so the
 // slow path reads the clock after every failed poll (each try_wait already
 // suspends the thread for a while): a wait that outlasts the bound always
@@ -138,15 +219,21 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------- geometry
-constexpr int kBM = 128;             // output rows per tile (tcgen05 M)
+// A CTA pair computes a 256 x 256 output tile: CTA rank r holds x rows
+// [m0 + 128 r, m0 + 128 r + 128) and W' rows (output columns) [n0 + 128 r, +128)
+// of every K stage; one thread of rank 0 issues 256 x 256 x 16 MMAs over both
+// CTAs' shared memory, and each CTA's TMEM receives its own 128 rows x 256 columns.
+constexpr int kBM = 128;             // output rows per CTA (TMEM lanes)
+constexpr int kPairM = 256;          // output rows per CTA pair (tcgen05 M, cta_group::2)
 constexpr int kBN = 256;             // output columns per tile (tcgen05 N)
+constexpr int kHalfN = kBN / 2;      // W' rows staged per CTA
 constexpr int kBK = 64;              // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
 constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi0 = 2;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr int kStageTx = kABytes + kBBytes;
+constexpr int kBBytes = kHalfN * kBK * 2;       // 16 KB
+constexpr int kStageTx = kABytes + kBBytes;     // bytes one CTA loads per stage
 constexpr int kBoxBytes = kBM * 64 * 2;         // one 128-row x 64-column bf16 store box
 constexpr int kSmA = 0;
 constexpr int kSmB = kSmA + kStages * kABytes;
@@ -163,8 +250,8 @@ enum : int { kSiteEmpty = 101, kSiteFull, kSiteAccEmpty, kSiteAccFull };
 
 struct GemmParams {
     int B, N, H, D, C, O;        // O = 3 H D output columns
-    int tiles_m, tiles_n, kb;    // row tiles per batch, column tiles, K stages per tile
-    long long total;             // B * tiles_m * tiles_n
+    int pairs_m, tiles_n, kb;    // 256-row blocks per batch, column tiles, K stages per tile
+    long long total;             // B * pairs_m * tiles_n pair tiles
     const float *inv_rms;        // [B * N]
     const float2 *rope;          // [D/2][N] (cos, sin)
     int *status;
@@ -235,20 +322,20 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 struct TileId {
-    int b, mt, nt;
+    int b, mp, nt;
 };
 __device__ __forceinline__ TileId tile_of(const GemmParams &p, long long t) {
-    const long long per_b = (long long)p.tiles_m * p.tiles_n;
+    const long long per_b = (long long)p.pairs_m * p.tiles_n;
     TileId id;
     id.b = (int)(t / per_b);
     const int rem = (int)(t - (long long)id.b * per_b);
-    id.mt = rem / p.tiles_n;     // column tiles fastest: concurrent CTAs share x rows
+    id.mp = rem / p.tiles_n;     // column tiles fastest: concurrent pairs share x rows
     id.nt = rem % p.tiles_n;
     return id;
 }
 
 // ---------------------------------------------------------------- the GEMM
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const GemmParams p) {
@@ -260,103 +347,107 @@ qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmBar + 8 * kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kSmBar + 8 * kNumBars + 4);
+    volatile uint32_t *peer_kc = reinterpret_cast<volatile uint32_t *>(smem + kSmBar + 8 * kNumBars + 8);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();
+    const bool lead = rank == 0;
     const uint64_t tlim = p.timeout_ns;
+    const long long npairs = gridDim.x / 2, pair = blockIdx.x / 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
+            // rank 0's barrier counts both CTAs' bytes; rank 1's is unused
             mbar_init(bar(kBarFull + s), 1);
             mbar_init(bar(kBarEmpty + s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(kBarAccFull + a), 1);
-            mbar_init(bar(kBarAccEmpty + a), 4);   // one arrival per epilogue warp
+            mbar_init(bar(kBarAccEmpty + a), 8);   // the epilogue warps of both CTAs
         }
         mbar_init(bar(kBarFinal), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(smem_addr(tmem_slot), 512);
-        tmem_relinquish();
+        tmem_alloc2(smem_addr(tmem_slot), 512);
+        tmem_relinquish2();
     }
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_w);
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // barriers of both CTAs initialised before any cross-CTA arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    uint32_t issued = 0;   // K stages this CTA's producer loaded
 
     if (warp == kWarpTma) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             uint32_t kc = 0;  // stages issued
             bool ok = true;
-            for (long long t = blockIdx.x; ok && t < p.total; t += gridDim.x) {
+            for (long long t = pair; ok && t < p.total; t += npairs) {
                 const TileId id = tile_of(p, t);
+                const int row = id.mp * kPairM + (int)rank * kBM;
+                const int col = id.nt * kBN + (int)rank * kHalfN;
                 for (int kb = 0; kb < p.kb; ++kb, ++kc) {
                     const int s = kc % kStages;
                     if (!(ok = wait1(bar(kBarEmpty + s), ((kc / kStages) & 1) ^ 1, abort_flag,
-                                         p.status, kSiteEmpty, tlim)))
+                                     p.status, kSiteEmpty, tlim)))
                         break;
-                    mbar_arrive_expect_tx(bar(kBarFull + s), kStageTx);
-                    tma_load_3d(sbase + kSmA + s * kABytes, &tm_x, bar(kBarFull + s), kb * kBK,
-                                id.mt * kBM, id.b);
-                    tma_load_2d(sbase + kSmB + s * kBBytes, &tm_w, bar(kBarFull + s), kb * kBK,
-                                id.nt * kBN);
+                    // both CTAs' bytes complete on rank 0's barrier
+                    if (lead) mbar_arrive_expect_tx(bar(kBarFull + s), 2 * kStageTx);
+                    const uint32_t fb = map_to_rank(bar(kBarFull + s), 0);
+                    tma_load_3d_pair(sbase + kSmA + s * kABytes, &tm_x, fb, kb * kBK, row, id.b);
+                    tma_load_2d_pair(sbase + kSmB + s * kBBytes, &tm_w, fb, kb * kBK, col);
                 }
             }
-            // drain: every copy this thread issued lands before the CTA exits
-            for (int s = 0; s < kStages; ++s) {
-                const uint32_t n = kc / kStages + ((uint32_t)s < kc % kStages ? 1u : 0u);
-                if (n > 0) drain_wait(bar(kBarFull + s), (n - 1) & 1, kDefaultWaitLimitNs);
-            }
+            issued = kc;
         }
     } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp follows the schedule; one elected lane issues. Each
-        // stage is four 128 x 256 x 16 MMAs whose descriptors differ only in
-        // the start address (32 bytes along K inside the swizzle atom).
-        const bool leader = elect_one();
-        const uint64_t dA = sdesc_sw128(sbase + kSmA, 16, 1024);
-        const uint64_t dB = sdesc_sw128(sbase + kSmB, 16, 1024);
-        constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false);
-        uint32_t kc = 0, tc = 0;
-        bool ok = true;
-        for (long long t = blockIdx.x; ok && t < p.total; t += gridDim.x, ++tc) {
-            const uint32_t buf = tc & 1, use = tc >> 1;
-            if (!(ok = wait_warp(bar(kBarAccEmpty + buf), (use & 1) ^ 1, abort_flag, p.status,
-                                      kSiteAccEmpty, tlim)))
-                break;
-            tc_fence_after();
-            const uint32_t d = tmem + buf * kBN;
-            for (int kb = 0; kb < p.kb; ++kb, ++kc) {
-                const int s = kc % kStages;
-                if (!(ok = wait_warp(bar(kBarFull + s), (kc / kStages) & 1, abort_flag, p.status,
-                                          kSiteFull, tlim)))
+        // ------------------------------------------------------------ MMA issuer (rank 0)
+        if (lead) {
+            const bool leader = elect_one();
+            const uint64_t dA = sdesc_sw128(sbase + kSmA, 16, 1024);
+            const uint64_t dB = sdesc_sw128(sbase + kSmB, 16, 1024);
+            constexpr uint32_t kIdesc = idesc_bf16(kPairM, kBN, false);
+            uint32_t kc = 0, tc = 0;
+            bool ok = true;
+            for (long long t = pair; ok && t < p.total; t += npairs, ++tc) {
+                const uint32_t buf = tc & 1, use = tc >> 1;
+                if (!(ok = wait_warp(bar(kBarAccEmpty + buf), (use & 1) ^ 1, abort_flag, p.status,
+                                     kSiteAccEmpty, tlim)))
                     break;
                 tc_fence_after();
-                if (leader) {
-                    const uint64_t a0 = dA + (uint64_t)(s * (kABytes >> 4));
-                    const uint64_t b0 = dB + (uint64_t)(s * (kBBytes >> 4));
+                const uint32_t d = tmem + buf * kBN;
+                for (int kb = 0; kb < p.kb; ++kb, ++kc) {
+                    const int s = kc % kStages;
+                    if (!(ok = wait_warp(bar(kBarFull + s), (kc / kStages) & 1, abort_flag, p.status,
+                                         kSiteFull, tlim)))
+                        break;
+                    tc_fence_after();
+                    if (leader) {
+                        const uint64_t a0 = dA + (uint64_t)(s * (kABytes >> 4));
+                        const uint64_t b0 = dB + (uint64_t)(s * (kBBytes >> 4));
 #pragma unroll
-                    for (int ks = 0; ks < kBK / 16; ++ks)
-                        mma_ss(d, a0 + ks * 2, b0 + ks * 2, kIdesc, (kb | ks) != 0 ? 1u : 0u);
-                    mma_commit(bar(kBarEmpty + s));
+                        for (int ks = 0; ks < kBK / 16; ++ks)
+                            mma2_ss(d, a0 + ks * 2, b0 + ks * 2, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                        mma2_commit_both(bar(kBarEmpty + s));
+                    }
+                    __syncwarp();
                 }
+                if (!ok) break;
+                if (leader) mma2_commit_both(bar(kBarAccFull + buf));
                 __syncwarp();
             }
-            if (!ok) break;
-            if (leader) mma_commit(bar(kBarAccFull + buf));
+            // drain: all issued MMAs complete (in both CTAs' TMEM) before the
+            // closing cluster barrier, after which both CTAs release TMEM
+            if (leader) mma2_commit_both(bar(kBarFinal));
             __syncwarp();
+            drain_wait(bar(kBarFinal), 0, kDefaultWaitLimitNs);
         }
-        // drain: all issued MMAs complete before TMEM is released
-        if (leader) mma_commit(bar(kBarFinal));
-        __syncwarp();
-        drain_wait(bar(kBarFinal), 0, kDefaultWaitLimitNs);
     } else {
         // ------------------------------------------------------------ epilogue
         const int qd = warp % 4;                     // TMEM lane quadrant of this warp
@@ -367,14 +458,17 @@ qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const uint32_t row_smem = sbase + kSmStage + (uint32_t)r * 128;
         const uint32_t swz = (uint32_t)(r & 7);
         uint32_t tc = 0;
-        for (long long t = blockIdx.x; t < p.total; t += gridDim.x, ++tc) {
+        // rank 1 hands its accumulator back on rank 0's barrier
+        const uint32_t acc_empty0 = lead ? bar(kBarAccEmpty) : map_to_rank(bar(kBarAccEmpty), 0);
+        for (long long t = pair; t < p.total; t += npairs, ++tc) {
             const TileId id = tile_of(p, t);
             const uint32_t buf = tc & 1, use = tc >> 1;
             const bool got = wait_warp(bar(kBarAccFull + buf), use & 1, abort_flag, p.status,
                                             kSiteAccFull, tlim);
             if (epi_sync_any(got ? 0u : 1u)) break;  // uniform over the four warps
             tc_fence_after();
-            const int n = id.mt * kBM + r;
+            const int row0 = id.mp * kPairM + (int)rank * kBM;   // first row of this CTA's half
+            const int n = row0 + r;
             const bool live = n < p.N;
             const float sc = live ? p.inv_rms[(long long)id.b * p.N + n] : 0.f;
             const uint32_t tacc = tmem + buf * kBN + lane_off;
@@ -432,18 +526,21 @@ qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     // every TMEM read of this accumulator is done: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kBarAccEmpty + buf));
+                    if (lane == 0) {
+                        if (lead) mbar_arrive(bar(kBarAccEmpty + buf));
+                        else mbar_arrive_remote(acc_empty0 + 8u * buf);
+                    }
                 }
                 fence_async_smem();
                 epi_sync();
-                if (store_thread) {
+                if (store_thread && row0 < p.N) {
 #pragma unroll 1
                     for (int bx = 0; bx < 2; ++bx) {
                         const int o = col0 + 64 * bx;       // first output column of the box
                         if (o >= p.O) continue;
                         const int part = o / HD, h = (o % HD) / p.D, d0 = o % p.D;
                         const CUtensorMap *m = part == 0 ? &tm_q : (part == 1 ? &tm_k : &tm_v);
-                        tma_store_4d(m, sbase + kSmStage + bx * kBoxBytes, d0, id.mt * kBM, h, id.b);
+                        tma_store_4d(m, sbase + kSmStage + bx * kBoxBytes, d0, row0, h, id.b);
                     }
                     bulk_commit();
                 }
@@ -452,11 +549,30 @@ qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if (store_thread) bulk_wait0();
     }
 
+    // Teardown. Every load of both CTAs completes on rank 0's stage barriers, so
+    // rank 0 drains them for both: rank 1 reports how many stages it loaded,
+    // and where an early exit left the two counts one phase apart rank 0
+    // supplies the missing expectation (rank 1's bytes arrive unexpected) or
+    // the missing bytes (rank 1 never loaded), then waits for the last phase.
+    if (!lead && warp == kWarpTma && lane == 0)
+        st_cluster_u32(map_to_rank(smem_addr(const_cast<uint32_t *>(peer_kc)), 0), issued);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // all roles done; MMAs drained; rank 1's count visible
+    if (lead && warp == kWarpTma && lane == 0) {
+        const uint32_t kc1 = *peer_kc;
+        for (int s = 0; s < kStages; ++s) {
+            const uint32_t n0 = issued / kStages + ((uint32_t)s < issued % kStages ? 1u : 0u);
+            const uint32_t n1 = kc1 / kStages + ((uint32_t)s < kc1 % kStages ? 1u : 0u);
+            if (n1 > n0) mbar_arrive_expect_tx(bar(kBarFull + s), kStageTx);
+            else if (n0 > n1) mbar_complete_tx(bar(kBarFull + s), kStageTx);
+            const uint32_t n = n0 > n1 ? n0 : n1;
+            if (n > 0) drain_wait(bar(kBarFull + s), (n - 1) & 1, kDefaultWaitLimitNs);
+        }
+    }
+    cluster_sync();   // no copy, arrival or MMA of either CTA is outstanding
     if (warp == kWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc2(tmem, 512);
     }
 }
 
@@ -504,15 +620,20 @@ cudaError_t prepare_gemm(int device) {
     return e;
 }
 
-int sm_count(int device) {
+// Co-resident CTA pairs of the GEMM on this device (one pair per two SMs
+// where the GPCs allow it): the persistent grid size.
+int max_pairs(int device) {
     static std::mutex mu;
     static int cache[64] = {};
     std::lock_guard<std::mutex> g(mu);
     if (device < 0 || device >= 64) return 0;
     if (cache[device] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmAlloc;
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess)
-            cache[device] = n;
+        if (cudaOccupancyMaxActiveClusters(&n, qkv_gemm_kernel, &cfg) == cudaSuccess) cache[device] = n;
     }
     return cache[device];
 }
@@ -630,7 +751,7 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
         const cuuint32_t xb[3] = {64, 128, 1};
         const cuuint64_t wd[2] = {(cuuint64_t)C, (cuuint64_t)O};
         const cuuint64_t ws[1] = {(cuuint64_t)C * 2};
-        const cuuint32_t wb[2] = {64, 256};
+        const cuuint32_t wb[2] = {64, (cuuint32_t)kHalfN};
         const cuuint32_t ob[4] = {64, 128, 1, 1};
         const cuuint64_t od[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
         bool ok = encode(&tx, x, 3, xd, xs, xb) && encode(&tw, w_folded, 2, wd, ws, wb);
@@ -657,18 +778,18 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
 
     GemmParams prm;
     prm.B = B; prm.N = N; prm.H = H; prm.D = D; prm.C = C; prm.O = (int)O;
-    prm.tiles_m = (N + kBM - 1) / kBM;
+    prm.pairs_m = (N + kPairM - 1) / kPairM;
     prm.tiles_n = (int)((O + kBN - 1) / kBN);
     prm.kb = (C + kBK - 1) / kBK;
-    prm.total = (long long)B * prm.tiles_m * prm.tiles_n;
+    prm.total = (long long)B * prm.pairs_m * prm.tiles_n;
     prm.inv_rms = inv_rms;
     prm.rope = reinterpret_cast<const float2 *>(rope);
     prm.status = reinterpret_cast<int *>(wsb);
     prm.timeout_ns = wait_limit_ns();
-    const int nsm = sm_count(dev);
-    if (nsm <= 0) { set_error("vdit_qkv_prologue: cannot query SM count"); return VDIT_ERR_CUDA; }
-    const long long grid = prm.total < nsm ? prm.total : nsm;
     VDIT_CUDA_TRY(prepare_gemm(dev));
+    const int pairs = max_pairs(dev);
+    if (pairs <= 0) { set_error("vdit_qkv_prologue: no CTA pair fits on this device"); return VDIT_ERR_CUDA; }
+    const long long grid = 2 * (prm.total < pairs ? prm.total : pairs);
     qkv_gemm_kernel<<<(unsigned)grid, kThreads, kSmAlloc, s>>>(tx, tw, tq, tk, tv, prm);
     VDIT_CUDA_TRY(cudaGetLastError());
     return VDIT_OK;
