@@ -223,6 +223,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 // [m0 + 128 r, m0 + 128 r + 128) and W' rows (output columns) [n0 + 128 r, +128)
 // of every K stage; one thread of rank 0 issues 256 x 256 x 16 MMAs over both
 // CTAs' shared memory, and each CTA's TMEM receives its own 128 rows x 256 columns.
+constexpr int kRmsThreads = 512;     // 1/rms pre-pass: 16 rows in flight per block
 constexpr int kBM = 128;             // output rows per CTA (TMEM lanes)
 constexpr int kPairM = 256;          // output rows per CTA pair (tcgen05 M, cta_group::2)
 constexpr int kBN = 256;             // output columns per tile (tcgen05 N)
@@ -285,8 +286,12 @@ __global__ void rope_table_kernel(float2 *table, int N, int D, double base) {
 // inv_rms[b*N + n] = 1 / sqrt(mean_c x[b, n, c]^2 + eps), one warp per row
 // (grid-stride over rows), 16-byte loads (C a multiple of 8), fp32
 // accumulation in a fixed order.
-__global__ void rms_kernel(const __nv_bfloat16 *x, long long xs0, long long xs1, int B, int N, int C,
-                           float eps, float *inv_rms) {
+__global__ void __launch_bounds__(kRmsThreads)
+rms_kernel(const __nv_bfloat16 *x, long long xs0, long long xs1, int B, int N, int C, float eps,
+           float *inv_rms) {
+    // The GEMM that consumes inv_rms may start now: only its epilogue waits
+    // for this grid (griddepcontrol.wait), its loads and MMAs overlap this pass.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x % 32;
     const long long rows = (long long)B * N;
     const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
@@ -295,6 +300,7 @@ __global__ void rms_kernel(const __nv_bfloat16 *x, long long xs0, long long xs1,
         const long long b = row / N, n = row % N;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + b * xs0 + n * xs1);
         float acc = 0.f;
+#pragma unroll 4
         for (int v = lane; v < C / 8; v += 32) {
             const uint4 u = src[v];
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
@@ -470,6 +476,7 @@ qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int row0 = id.mp * kPairM + (int)rank * kBM;   // first row of this CTA's half
             const int n = row0 + r;
             const bool live = n < p.N;
+            if (tc == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // 1/rms pre-pass done
             const float sc = live ? p.inv_rms[(long long)id.b * p.N + n] : 0.f;
             const uint32_t tacc = tmem + buf * kBN + lane_off;
             const int col_t = id.nt * kBN;
@@ -618,6 +625,19 @@ cudaError_t prepare_gemm(int device) {
         cudaFuncSetAttribute(qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
     if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
     return e;
+}
+
+int sm_count(int device) {
+    static std::mutex mu;
+    static int cache[64] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (device < 0 || device >= 64) return 0;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess)
+            cache[device] = n;
+    }
+    return cache[device];
 }
 
 // Co-resident CTA pairs of the GEMM on this device (one pair per two SMs
@@ -772,8 +792,13 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const long long rows = (long long)B * N;
-    rms_kernel<<<grid_for(rows * 32, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                        x_strides[0], x_strides[1], B, N, C, eps, inv_rms);
+    // One resident block per SM (grid-stride over rows), small enough to share
+    // each SM with a GEMM CTA, which launches as soon as every block has started.
+    const int nsm = sm_count(dev);
+    if (nsm <= 0) { set_error("vdit_qkv_prologue: cannot query SM count"); return VDIT_ERR_CUDA; }
+    const long long rms_blocks = (rows + kRmsThreads / 32 - 1) / (kRmsThreads / 32);
+    rms_kernel<<<(unsigned)(rms_blocks < nsm ? rms_blocks : nsm), kRmsThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(x), x_strides[0], x_strides[1], B, N, C, eps, inv_rms);
     VDIT_CUDA_TRY(cudaGetLastError());
 
     GemmParams prm;
@@ -790,8 +815,18 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
     const int pairs = max_pairs(dev);
     if (pairs <= 0) { set_error("vdit_qkv_prologue: no CTA pair fits on this device"); return VDIT_ERR_CUDA; }
     const long long grid = 2 * (prm.total < pairs ? prm.total : pairs);
-    qkv_gemm_kernel<<<(unsigned)grid, kThreads, kSmAlloc, s>>>(tx, tw, tq, tk, tv, prm);
-    VDIT_CUDA_TRY(cudaGetLastError());
+    // Programmatic dependent launch on the pre-pass (cluster shape from the kernel).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    VDIT_CUDA_TRY(cudaLaunchKernelEx(&cfg, qkv_gemm_kernel, tx, tw, tq, tk, tv, prm));
     return VDIT_OK;
 }
 
