@@ -300,9 +300,7 @@ rms_kernel(const __nv_bfloat16 *x, long long xs0, long long xs1, int B, int N, i
         const long long b = row / N, n = row % N;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + b * xs0 + n * xs1);
         float acc = 0.f;
-#pragma unroll 4
-        for (int v = lane; v < C / 8; v += 32) {
-            const uint4 u = src[v];
+        auto add_sq = [&](const uint4 &u) {
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -310,7 +308,19 @@ rms_kernel(const __nv_bfloat16 *x, long long xs0, long long xs1, int B, int N, i
                 acc = fmaf(lo, lo, acc);
                 acc = fmaf(hi, hi, acc);
             }
+        };
+        // batches of 8 independent 16-byte loads per lane (64 KB in flight per
+        // SM at 16 warps), then the remainder one load at a time
+        const int nv = C / 8;
+        int v0 = 0;
+        for (; v0 + 32 * 8 <= nv; v0 += 32 * 8) {
+            uint4 u[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) u[j] = __ldg(src + v0 + 32 * j + lane);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) add_sq(u[j]);
         }
+        for (int v = v0 + lane; v < nv; v += 32) add_sq(__ldg(src + v));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         if (lane == 0) inv_rms[row] = 1.0f / sqrtf(acc / (float)C + eps);
