@@ -30,7 +30,8 @@ EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_p
             "vdit_attn_fwd", "vdit_last_error", "vdit_version", "vdit_key_stats_noalloc",
             "vdit_set_wait_limit_ns", "vdit_key_stats_framed_workspace_size",
             "vdit_key_stats_framed", "vdit_attn_fwd_framed", "vdit_qkv_fold_gamma",
-            "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status")
+            "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status",
+            "vdit_pipeline_create", "vdit_pipeline_run", "vdit_pipeline_destroy")
 
 
 class VditError(RuntimeError):
@@ -107,6 +108,12 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_qkv_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         for fn in ("vdit_qkv_fold_gamma", "vdit_rope_table", "vdit_qkv_prologue", "vdit_qkv_status"):
             getattr(lib, fn).restype = ctypes.c_int
+        lib.vdit_pipeline_create.argtypes = [vp, i32, i32, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.vdit_pipeline_create.restype = ctypes.c_int
+        lib.vdit_pipeline_run.argtypes = [vp, vp, vp, vp, vp, vp, _I64x3, f32, f32, i32, vp]
+        lib.vdit_pipeline_run.restype = ctypes.c_int
+        lib.vdit_pipeline_destroy.argtypes = [vp]
+        lib.vdit_pipeline_destroy.restype = None
         _lib = lib
         return lib
 
@@ -410,6 +417,62 @@ def qkv_status(workspace, stream=None) -> int:
     code = ctypes.c_int32(0)
     load_library().vdit_qkv_status(_ptr(workspace), _stream(stream), ctypes.byref(code))
     return code.value
+
+
+class Pipeline:
+    """Head-group pipelined attention over HOST tensors ("Hiding the Collective",
+    Fig. 2): each group of heads is copied in, gets its key statistics and
+    attention, and is copied out, on three streams, so the middle transfers
+    hide behind other groups' attention (vdit_pipeline_*)."""
+
+    def __init__(self, plan: "Plan", B, H, D, groups):
+        """groups: a count (equal split), 0 (the library's tapered schedule) or a
+        sequence of per-group head counts."""
+        lib = load_library()
+        h = ctypes.c_void_p()
+        sizes = None
+        if not isinstance(groups, int):
+            sizes = (ctypes.c_int32 * len(groups))(*[int(g) for g in groups])
+            groups = len(groups)
+        _check(lib.vdit_pipeline_create(plan.handle, int(B), int(H), int(D), int(groups),
+                                        ctypes.cast(sizes, ctypes.c_void_p) if sizes is not None else None,
+                                        ctypes.byref(h)))
+        self._h = h
+        self.plan = plan            # the pipeline keeps using the plan's device schedule
+        self.B, self.H, self.D, self.groups = int(B), int(H), int(D), groups
+
+    def run(self, q_h, k_h, v_h, o_h, scale, lse_h=None, tau=64.0, mode="auto", stream=None):
+        """q_h, k_h, v_h, o_h: bf16 CPU tensors (pinned for overlap) indexed
+        [B, H, N, D] with identical strides and d contiguous; lse_h: optional fp32
+        [B, H, N] contiguous CPU tensor. Asynchronous: synchronise the stream
+        before reading o_h."""
+        import torch
+        ts = (q_h, k_h, v_h, o_h)
+        for name, t in zip("qkvo", ts):
+            if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or t.dtype != torch.bfloat16:
+                raise ValueError(f"{name}_h must be a 4-D bf16 CPU tensor")
+            if t.stride() != q_h.stride() or t.shape != q_h.shape or t.stride(3) != 1:
+                raise ValueError("host tensors must share shape and strides, with d contiguous")
+        if tuple(q_h.shape) != (self.B, self.H, self.plan.num_tokens, self.D):
+            raise ValueError("host tensors do not match the pipeline's B, H, N, D")
+        if lse_h is not None and (lse_h.dtype != torch.float32 or not lse_h.is_contiguous()
+                                  or tuple(lse_h.shape) != (self.B, self.H, self.plan.num_tokens)):
+            raise ValueError("lse_h must be a contiguous fp32 [B, H, N] CPU tensor")
+        _check(load_library().vdit_pipeline_run(
+            self._h, _ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h), _strides(q_h),
+            float(scale), float(tau), MODES[mode], _stream(stream)))
+        return o_h
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            load_library().vdit_pipeline_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def set_wait_limit_ns(ns: int) -> None:

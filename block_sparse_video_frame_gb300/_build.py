@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvdit.so")
-SOURCES = ["vdit_api.cu", "vdit_plan.cu", "vdit_stats.cu", "vdit_attn.cu", "vdit_prologue.cu"]
+SOURCES = ["vdit_api.cu", "vdit_plan.cu", "vdit_stats.cu", "vdit_attn.cu", "vdit_prologue.cu", "vdit_pipeline.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

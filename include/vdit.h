@@ -286,6 +286,56 @@ VDIT_API vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[2]
  * word was 0, VDIT_ERR_TIMEOUT otherwise. */
 VDIT_API vdit_status vdit_qkv_status(void *workspace, void *stream, int32_t *code);
 
+/* ---------------------------------------------------------------------------
+ * Head-group pipelining over host-resident tensors ("Hiding the Collective",
+ * Fig. 2). The pages split attention's heads into independent groups, each
+ * with its own transfer -> attention -> transfer chain, so that every middle
+ * transfer hides behind another group's attention and only the first transfer
+ * in and the last transfer out stay exposed. Splitting by heads leaves the
+ * token order, and so the mask, unchanged: grouped results equal ungrouped
+ * ones bit for bit. Here the transfer is the host link of one GPU: a pipeline
+ * copies each group's Q, K, V in, runs vdit_key_stats and vdit_attn_fwd on it,
+ * and copies its O (and LSE) out, on internal streams ordered by events, with
+ * two device slots in turn.
+ * ------------------------------------------------------------------------- */
+typedef struct vdit_pipeline vdit_pipeline;
+
+/* Create a pipeline for attention with `plan` over B x H heads of size D, split
+ * into `groups` head groups: group_heads[g] heads each (host array of `groups`
+ * positive counts summing to H), or, when group_heads is NULL, ceil(H / groups)
+ * heads each (the last may be smaller). groups = 0 with group_heads NULL picks
+ * a tapered schedule: 1, 2, 3 heads, then groups of 4 (one more head in the
+ * first ones when 4 does not divide the rest), then 3, 2, 1 heads, so that the
+ * exposed first copy-in and last copy-out are one head each; for H < 16 an
+ * even split into groups of about 4. Allocates two device slots (Q, K, V, O,
+ * LSE, statistics and their workspace for the largest group each), four streams
+ * and the events; owns them until vdit_pipeline_destroy. Errors:
+ * VDIT_ERR_INVALID (null plan or out, B or H < 1, groups outside [0, H], bad
+ * group_heads, plan from another device), VDIT_ERR_UNSUPPORTED (D),
+ * VDIT_ERR_NOMEM, VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int32_t H, int32_t D,
+                                          int32_t groups, const int32_t *group_heads,
+                                          vdit_pipeline **out);
+
+/* Run attention on HOST tensors: q_host, k_host, v_host (bf16, read) and o_host
+ * (bf16, written) share the element strides host_strides for (b, h, n), with d
+ * contiguous; lse_host (fp32 [B, H, N] dense) may be NULL. Host memory should be
+ * pinned (page-locked) for the copies to overlap the kernels. Key statistics
+ * use tau as in vdit_key_stats; mode as in vdit_attn_fwd. Asynchronous with
+ * respect to the host: the work is ordered after everything already queued on
+ * `stream`, and `stream` waits for all of it, so a synchronisation of `stream`
+ * means o_host (and lse_host) are complete. An expired wait inside attention
+ * is reported by vdit_plan_status on the plan. Errors: VDIT_ERR_INVALID,
+ * VDIT_ERR_CUDA, and those of vdit_key_stats and vdit_attn_fwd. */
+VDIT_API vdit_status vdit_pipeline_run(vdit_pipeline *pipeline, const void *q_host,
+                                       const void *k_host, const void *v_host, void *o_host,
+                                       float *lse_host, const int64_t host_strides[3], float scale,
+                                       float tau, int32_t mode, void *stream);
+
+/* Wait for the pipeline's streams, then free its device memory, streams and
+ * events. NULL is ignored. */
+VDIT_API void vdit_pipeline_destroy(vdit_pipeline *pipeline);
+
 /* Failure-detection test hook. Every wait inside the attention kernel and the
  * prologue GEMM is bounded; when a wait expires the kernel records which wait
  * in its status word (the plan's, or the prologue workspace's), drains its

@@ -100,3 +100,37 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "vdit_oracle" not in text, f
+
+
+def test_pipeline_entry_points_reject_bad_arguments(lib):
+    h = ctypes.c_void_p(1234)
+    assert lib.vdit_pipeline_create(None, 1, 8, 128, 2, None, ctypes.byref(h)) == vd.VDIT_ERR_INVALID
+    assert "plan" in lib.vdit_last_error().decode()
+    assert not h.value
+    assert lib.vdit_pipeline_create(ctypes.c_void_p(0x1000), 1, 8, 128, 2, None, None) == vd.VDIT_ERR_INVALID
+    sizes = (ctypes.c_int32 * 2)(3, 4)     # sums to 7, not H = 8
+    fake_plan = ctypes.c_void_p(0x1000)
+    assert lib.vdit_pipeline_create(fake_plan, 1, 8, 128, 2, sizes, ctypes.byref(h)) == vd.VDIT_ERR_INVALID
+    assert "sum" in lib.vdit_last_error().decode()
+    s3 = vd._I64x3(8, 8, 8)
+    p = ctypes.c_void_p(0x1000)
+    assert lib.vdit_pipeline_run(None, p, p, p, p, None, s3, 0.1, 64.0, 0, None) == vd.VDIT_ERR_INVALID
+    lib.vdit_pipeline_destroy(None)   # NULL is ignored
+
+
+def test_prologue_entry_points_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(0x1000)
+    s2 = (ctypes.c_int64 * 2)(1024, 1024)
+    s3 = vd._I64x3(8, 8, 8)
+    st = lib.vdit_qkv_prologue(None, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1024, 8, 128, 1e-6, p, 1 << 20, None)
+    assert st == vd.VDIT_ERR_INVALID and "NULL" in lib.vdit_last_error().decode()
+    st = lib.vdit_qkv_prologue(p, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1024, 8, 96, 1e-6, p, 1 << 20, None)
+    assert st == vd.VDIT_ERR_UNSUPPORTED
+    st = lib.vdit_qkv_prologue(p, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1020, 8, 128, 1e-6, p, 1 << 20, None)
+    assert st == vd.VDIT_ERR_INVALID and "multiple of 8" in lib.vdit_last_error().decode()
+    st = lib.vdit_qkv_prologue(p, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1024, 8, 128, 1e-6, p, 16, None)
+    assert st == vd.VDIT_ERR_INVALID and "workspace" in lib.vdit_last_error().decode()
+    assert lib.vdit_qkv_workspace_size(1, 46800) >= 46800 * 4
+    assert lib.vdit_rope_table(None, 16, 128, 1e4, None) == vd.VDIT_ERR_INVALID
+    assert lib.vdit_rope_table(p, 16, 127, 1e4, None) == vd.VDIT_ERR_INVALID
+    assert lib.vdit_qkv_fold_gamma(None, p, p, 4, 8, None) == vd.VDIT_ERR_INVALID
