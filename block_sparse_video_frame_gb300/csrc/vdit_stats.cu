@@ -43,6 +43,9 @@ struct StatsArgs {
 // kUnroll such loads per tensor in flight.
 constexpr int kUnroll = 4;
 
+__device__ __forceinline__ uint4 load16(const __nv_bfloat16 *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
 __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
     const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -51,6 +54,11 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
         x[2 * e] = __uint_as_float(w[e] << 16);
         x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
+}
+// bf16 element e (0..7) of a 16-byte load, as fp32 (exact)
+__device__ __forceinline__ float elem8(const uint4 &u, int e) {
+    const uint32_t w = e < 2 ? u.x : e < 4 ? u.y : e < 6 ? u.z : u.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -67,7 +75,7 @@ __device__ __forceinline__ float row_sum(float v) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
+__global__ void __launch_bounds__(kStatsThreads, 4) stats_pass1(StatsArgs a) {
     constexpr int LPR = D / 8;          // lanes per row
     constexpr int RPW = 32 / LPR;       // rows per warp-wide load
     __shared__ float s_col[kStatsWarps * RPW][D];
@@ -86,25 +94,29 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass1(StatsArgs a) {
     // warp-uniform loop bound: every lane runs the same iterations (the row
     // sums below shuffle across the whole warp); rows past the chunk load zeros
     for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll) {
-        float xk[kUnroll][8], xq[kUnroll][8];
+        // raw 16-byte loads stay packed until used (few registers, more
+        // blocks per SM, more loads in flight)
+        uint4 xk[kUnroll], xq[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int r = wbase + sub + u * kStep;
             if (r < r1) {
-                load8(kb + (long long)r * a.ks2, xk[u]);
-                load8(qb + (long long)r * a.qs2, xq[u]);
+                xk[u] = load16(kb + (long long)r * a.ks2);
+                xq[u] = load16(qb + (long long)r * a.qs2);
             } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xk[u][e] = xq[u][e] = 0.f;
+                xk[u] = xq[u] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += xk[u][e];
+            for (int e = 0; e < 8; ++e) acc[e] += elem8(xk[u], e);
             float sq = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sq = fmaf(xq[u][e], xq[u][e], sq);
+            for (int e = 0; e < 8; ++e) {
+                const float x = elem8(xq[u], e);
+                sq = fmaf(x, x, sq);
+            }
             qm2 = fmaxf(qm2, row_sum<LPR>(sq));
         }
     }
