@@ -61,6 +61,9 @@ def parse_args(argv=None):
                          "(0: the library's tapered schedule)")
     ap.add_argument("--pipeline-sweep", action="store_true",
                     help="end-to-end time over host tensors per head-group count; one JSON line each")
+    ap.add_argument("--bs-sweep", action="store_true",
+                    help="schedule block size sweep on one workload: plan build time, CSR size and "
+                         "attention time per valid block size; one JSON line each")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the one-line contract: time the attention call on every "
                          "workload and the dense eligibility sweep in AUTO, ONLINE and STATIC "
@@ -388,6 +391,51 @@ def run_prologue(args):
     return 0
 
 
+def run_bs_sweep(args):
+    """"Deleting the Mask" asks for a block size that is a multiple of 16 and
+    divides the frame's token span. Here the block size only shapes the
+    reported CSR schedule: the kernel walks each frame's key runs in 128-key
+    tiles whatever the block size, so attention time should not depend on it.
+    Per valid block size: plan rebuild time (2 kernels), nnz, live pairs and
+    the attention call's time."""
+    import torch
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+    torch.cuda.set_device(0)
+    vd.load_library()
+    w = configs.BY_NAME[args.workload]
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    st = vd.key_stats(q, k, w.scale)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    sizes = [bs for bs in range(16, w.T + 1, 16) if w.T % bs == 0] if not w.dense else [16, 128, 1024]
+    for bs in sizes:
+        plan = vd.attn_plan(w.F, w.T, w.W, w.ref, bs)
+        plan_ms = timed(lambda: plan.rebuild(), 20)
+        attn_ms = timed(lambda: vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False), 10)
+        if plan.status() != 0:
+            raise RuntimeError(f"expired wait at bs={bs}")
+        flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
+        print(json.dumps({"workload": w.name, "block_size": bs, "nnz_blocks": int(plan.info.nnz),
+                          "live_pairs_per_head": plan.live_pairs, "plan_rebuild_ms": plan_ms,
+                          "attn_ms": attn_ms, "attn_tflops": flops / (attn_ms * 1e-3) / 1e12}), flush=True)
+        plan.close()
+    return 0
+
+
 def run_pipeline_sweep(args):
     """"Hiding the Collective" on one GPU: end-to-end time of the attention call
     over pinned host Q, K, V, O per head-group count G (G = 1 is the monolithic
@@ -452,6 +500,8 @@ def main(argv=None):
         return run_prologue(args)
     if args.pipeline_sweep:
         return run_pipeline_sweep(args)
+    if args.bs_sweep:
+        return run_bs_sweep(args)
 
     import torch
     import torch.distributed as dist
