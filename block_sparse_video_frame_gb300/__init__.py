@@ -31,7 +31,8 @@ EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_p
             "vdit_set_wait_limit_ns", "vdit_key_stats_framed_workspace_size",
             "vdit_key_stats_framed", "vdit_attn_fwd_framed", "vdit_qkv_fold_gamma",
             "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status",
-            "vdit_pipeline_create", "vdit_pipeline_run", "vdit_pipeline_destroy")
+            "vdit_pipeline_create", "vdit_pipeline_run", "vdit_pipeline_destroy",
+            "vdit_set_alloc_fail_after")
 
 
 class VditError(RuntimeError):
@@ -114,6 +115,8 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_pipeline_run.restype = ctypes.c_int
         lib.vdit_pipeline_destroy.argtypes = [vp]
         lib.vdit_pipeline_destroy.restype = None
+        lib.vdit_set_alloc_fail_after.argtypes = [i32]
+        lib.vdit_set_alloc_fail_after.restype = None
         _lib = lib
         return lib
 
@@ -473,6 +476,12 @@ class Pipeline:
             self.close()
         except Exception:
             pass
+
+
+def set_alloc_fail_after(n: int) -> None:
+    """Test hook: the n-th device allocation the library makes from now on fails
+    once (VDIT_ERR_NOMEM); n <= 0 switches it off (vdit_set_alloc_fail_after)."""
+    load_library().vdit_set_alloc_fail_after(int(n))
 
 
 def set_wait_limit_ns(ns: int) -> None:

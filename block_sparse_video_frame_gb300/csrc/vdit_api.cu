@@ -14,6 +14,24 @@ std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+namespace {
+std::atomic<int> g_fail_after{0};   // > 0: allocations left until the one that fails
+}
+
+cudaError_t device_alloc(void **ptr, size_t bytes) {
+    int n = g_fail_after.load(std::memory_order_relaxed);
+    while (n > 0) {
+        if (g_fail_after.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) {
+            if (n == 1) {
+                *ptr = nullptr;
+                return cudaErrorMemoryAllocation;
+            }
+            break;
+        }
+    }
+    return cudaMalloc(ptr, bytes);
+}
+
 void set_error(const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -34,6 +52,10 @@ extern "C" const char *vdit_last_error(void) { return vdit::g_err; }
 
 extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {
     vdit::g_wait_limit_ns.store(ns == 0 ? vdit::kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+}
+
+extern "C" void vdit_set_alloc_fail_after(int32_t n) {
+    vdit::g_fail_after.store(n > 0 ? n : 0, std::memory_order_relaxed);
 }
 
 extern "C" const char *vdit_version(void) { return "libvdit 0.1 (sm_103a, tcgen05)"; }

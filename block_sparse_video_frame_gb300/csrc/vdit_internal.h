@@ -29,6 +29,10 @@ vdit_status cuda_fail(cudaError_t e, const char *what);
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
 unsigned long long wait_limit_ns();
 
+// cudaMalloc behind the allocation-failure test hook (vdit_set_alloc_fail_after):
+// every device allocation the library makes goes through here.
+cudaError_t device_alloc(void **ptr, size_t bytes);
+
 // Query-tile geometry shared by the plan and the attention kernel.
 constexpr int kTileRows = 128;   // rows of one query tile (tcgen05 M)
 constexpr int kTilesPerUnit = 2; // query tiles that share one K/V stream

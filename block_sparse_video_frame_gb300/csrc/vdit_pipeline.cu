@@ -226,10 +226,10 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
                               align_up((size_t)B * hg);
     const size_t ws_bytes = align_up(vdit_key_stats_workspace_size(B, p->hg, p->N, D));
     const size_t per_slot = 4 * t_bytes + lse_bytes + stat_bytes + ws_bytes;
-    cudaError_t e = cudaMalloc(&p->mem, per_slot * kSlots);
+    cudaError_t e = device_alloc(&p->mem, per_slot * kSlots);
     if (e != cudaSuccess) {
         release(p);
-        set_error("vdit_pipeline_create: cudaMalloc of %zu bytes failed (%s)", per_slot * kSlots,
+        set_error("vdit_pipeline_create: device allocation of %zu bytes failed (%s)", per_slot * kSlots,
                   cudaGetErrorString(e));
         return VDIT_ERR_NOMEM;
     }

@@ -252,12 +252,12 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
     p->units_cap = (int)(p->N / (kTileRows * kTilesPerUnit)) + 2 * F + 2;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
-    e = cudaMalloc(&p->d_header, sizeof(PlanHeader));
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_frame_runs, sizeof(int32_t) * 4 * F);
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_segments, sizeof(int32_t) * kSegInts * F);
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_units, sizeof(int32_t) * p->units_cap);
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_class_off, sizeof(int32_t) * (kMaxClasses + 1));
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
+    e = device_alloc(reinterpret_cast<void **>(&p->d_header), sizeof(PlanHeader));
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_frame_runs), sizeof(int32_t) * 4 * F);
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_segments), sizeof(int32_t) * kSegInts * F);
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_units), sizeof(int32_t) * p->units_cap);
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_class_off), sizeof(int32_t) * (kMaxClasses + 1));
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_status), sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) {
         free_plan_buffers(p);
@@ -280,8 +280,8 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
         delete p;
         return VDIT_ERR_INVALID;
     }
-    e = cudaMalloc(&p->d_row_ptr, sizeof(int32_t) * (p->n_qblocks + 1));
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_col_idx, sizeof(int32_t) * (p->h.nnz > 0 ? p->h.nnz : 1));
+    e = device_alloc(reinterpret_cast<void **>(&p->d_row_ptr), sizeof(int32_t) * (p->n_qblocks + 1));
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_col_idx), sizeof(int32_t) * (p->h.nnz > 0 ? p->h.nnz : 1));
     if (e != cudaSuccess) {
         free_plan_buffers(p);
         delete p;

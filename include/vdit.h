@@ -347,6 +347,13 @@ VDIT_API void vdit_pipeline_destroy(vdit_pipeline *pipeline);
  * keeps the default bound. */
 VDIT_API void vdit_set_wait_limit_ns(uint64_t ns);
 
+/* Allocation-failure test hook. With n >= 1, the n-th device allocation the
+ * library makes from now on (counted process-wide; plan and pipeline creation
+ * allocate) fails as if the device were out of memory, once; the call that
+ * made it frees what it had allocated and returns VDIT_ERR_NOMEM. n <= 0
+ * switches the hook off. For tests of the error paths; no fault is involved. */
+VDIT_API void vdit_set_alloc_fail_after(int32_t n);
+
 /* Thread-local, library-owned text of the last error on this thread ("" if none). */
 VDIT_API const char *vdit_last_error(void);
 
