@@ -98,3 +98,20 @@ def test_pipeline_full_size_720p_groups():
     assert plan.status() == 0
     assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
     assert torch.equal(lse_h, lse_ref)
+
+
+@pytest.mark.parametrize("w,groups", [(configs.SMALL.with_(name="small_b2", B=2, seed=21), 3),
+                                      (configs.TINY, 2)], ids=["b2_d128", "d64"])
+def test_pipeline_batches_and_head_dim_64(w, groups):
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    o_ref, lse_ref = device_reference(w, q, k, v, plan)
+    q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+    o_h = pinned_like(q)
+    lse_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
+    pipe = vd.Pipeline(plan, w.B, w.H, w.D, groups)
+    pipe.run(q_h, k_h, v_h, o_h, w.scale, lse_h=lse_h)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse_h, lse_ref)
