@@ -26,6 +26,10 @@
 // so one warpgroup's exponentials overlap the other's MMAs. TMEM (512 cols):
 // O0 | O1 | S0 | S1; P (bf16, two per 32-bit column) overwrites the first half
 // of its S buffer and is the A operand (from TMEM) of the P.V MMA.
+// A segment with an odd number of tiles ends in a lone tile. On the static path
+// its key tiles alternate between both slots (both read the same Q tile), so
+// it overlaps like a pair; the epilogue adds O0 + O1 and the two row sums,
+// exact because both halves share the static bound.
 // Every wait is bounded in time; on expiry the CTA records a site code in the
 // plan's status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -76,7 +80,7 @@ __device__ __forceinline__ void static_for(F &&f) {
 // status-word site codes (which wait expired)
 enum : int {
     kSiteQfree = 1, kSiteKfree, kSiteVfree, kSiteQfullMma, kSiteKfull, kSiteVfull, kSitePfull,
-    kSiteOfree, kSiteQfullSm, kSiteSfull, kSiteOfull, kSiteDrain
+    kSiteOfree, kSiteQfullSm, kSiteSfull, kSiteOfull, kSiteDrain, kSiteXfull, kSiteXfree
 };
 
 template <int D>
@@ -86,7 +90,8 @@ struct Layout {
     static constexpr int kK = kQ + kTilesPerUnit * kTileBytes;
     static constexpr int kV = kK + kStagesK * kTileBytes;
     static constexpr int kBar = kV + kStagesV * kTileBytes;
-    static constexpr int kBytes = kBar + 256;
+    static constexpr int kX = kBar + 256;          // row sums handed between warpgroups
+    static constexpr int kBytes = kX + kTileRows * 4;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemO = 0;         // O0 at col 0, O1 at col D
     static constexpr uint32_t kTmemS = 2 * D;     // S0 at 2D, S1 at 2D + 128
@@ -96,7 +101,7 @@ struct Layout {
 enum : int {
     kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = 4, kBarVfull = 6, kBarVfree = 9,
     kBarSfull = 12, kBarPfull = 14, kBarOfull = 16, kBarOfree = 18, kBarFinal = 20,
-    kNumBars = 21
+    kBarXfull = 21, kBarXfree = 22, kNumBars = 23
 };
 
 struct Params {
@@ -126,6 +131,8 @@ struct Work {
     int seg, pair, ntile;  // segment, this unit's tile pair, tiles in the segment
     int nact;              // active query tiles (1 or 2)
     int nt0, nkt;          // key tiles of run 0, total key tiles
+    bool stat;             // static-max softmax (else online)
+    bool alt;              // lone static tile: slots 0 and 1 take alternate key tiles
 };
 
 __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
@@ -153,6 +160,14 @@ __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
     u.nact = min(kTilesPerUnit, u.ntile - kTilesPerUnit * u.pair);
     u.nt0 = (u.hi0 - u.lo0 + kBK - 1) / kBK;
     u.nkt = u.nt0 + (u.hi1 - u.lo1 + kBK - 1) / kBK;
+    u.stat = p.mode == VDIT_MODE_FORCE_STATIC ||
+             (p.mode == VDIT_MODE_AUTO &&
+              (p.seg_elig ? p.seg_elig[(size_t)u.bh * p.nseg + u.seg] : p.elig[u.bh]) != 0);
+    // A lone tile has no partner to overlap its softmax with. On the static path
+    // its key tiles alternate between both slots (even ones in slot 0, odd ones
+    // in slot 1, both reading the same Q tile): the bound is common to both
+    // halves, so O = O0 + O1 and l = l0 + l1 exactly, with no rescale.
+    u.alt = u.nact == 1 && u.nkt >= 2 && u.stat;
 }
 
 // first row of query tile q of the unit (last tile of a segment ends at its end)
@@ -220,6 +235,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(kBarOfree + q), 4);
         }
         mbar_init(bar(kBarFinal), 1);
+        mbar_init(bar(kBarXfull), 4);   // row sums of slot 1, passed to warpgroup 0
+        mbar_init(bar(kBarXfree), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -305,8 +322,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
         constexpr uint32_t kIdescS = idesc_bf16(128, kBK, false);
         // S_q = Q_q K^T (K-major A and B); a tail tile uses a narrower N
-        auto issue_s = [&](int q, int sk, int nmma) {
-            const uint64_t a0 = dQ + (uint64_t)(q * kTileDesc);
+        auto issue_s = [&](int q, int sk, int nmma, int qt) {   // slot q, Q tile qt
+            const uint64_t a0 = dQ + (uint64_t)(qt * kTileDesc);
             const uint64_t b0 = dK + (uint64_t)(sk * kTileDesc);
             const uint32_t idesc = nmma == kBK ? kIdescS : idesc_bf16(128, nmma, false);
             const uint32_t d = tS0 + q * 128;
@@ -337,14 +354,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!(ok = wait(kBarQfull, it & 1, kSiteQfullMma))) break;
             const uint32_t kc0 = kc;
             int start, nvalid;
+            if (u.alt) {
+                // slot j % 2 takes key tile j: S of key tiles 0 and 1, then per key
+                // tile j its P.V and the S of key tile j + 2 into the same slot
+#pragma unroll
+                for (int q = 0; q < kTilesPerUnit; ++q) {
+                    const uint32_t c = kc0 + q;
+                    const int sk = c % kStagesK;
+                    key_tile(u, q, start, nvalid);
+                    if (!(ok = wait(kBarKfull + sk, (c / kStagesK) & 1, kSiteKfull))) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_s(q, sk, (nvalid + 15) & ~15, 0);
+                        mma_commit(bar(kBarSfull + q));
+                    }
+                    __syncwarp();
+                }
+                for (int j = 0; j < u.nkt && ok; ++j) {
+                    const int q = j & 1;
+                    const uint32_t c = kc0 + j;
+                    const int sv = c % kStagesV;
+                    key_tile(u, j, start, nvalid);
+                    const int nmma = (nvalid + 15) & ~15;
+                    if (!(ok = wait(kBarVfull + sv, (c / kStagesV) & 1, kSiteVfull))) break;
+                    if (!(ok = wait(kBarPfull + q, sq[q] & 1, kSitePfull))) break;
+                    if (j == q && !(ok = wait(kBarOfree + q, (uq[q] & 1) ^ 1, kSiteOfree))) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_pv(q, sv, nmma, j >= 2);
+                        if (j + 2 >= u.nkt) mma_commit(bar(kBarOfull + q));
+                    }
+                    ++sq[q];
+                    if (j + 2 < u.nkt) {
+                        const uint32_t c2 = c + 2;
+                        const int sk2 = c2 % kStagesK;
+                        int start2, nvalid2;
+                        key_tile(u, j + 2, start2, nvalid2);
+                        if (!(ok = wait(kBarKfull + sk2, (c2 / kStagesK) & 1, kSiteKfull))) break;
+                        tc_fence_after();
+                        if (leader) {
+                            issue_s(q, sk2, (nvalid2 + 15) & ~15, 0);
+                            mma_commit(bar(kBarSfull + q));
+                        }
+                    }
+                    __syncwarp();
+                }
+                ++uq[0];
+                ++uq[1];
+                kc += u.nkt;
+                continue;
+            }
             key_tile(u, 0, start, nvalid);
+
             {
                 const int sk = kc0 % kStagesK;
                 if (!(ok = wait(kBarKfull + sk, (kc0 / kStagesK) & 1, kSiteKfull))) break;
                 tc_fence_after();
                 if (leader) {
                     for (int q = 0; q < u.nact; ++q) {
-                        issue_s(q, sk, (nvalid + 15) & ~15);
+                        issue_s(q, sk, (nvalid + 15) & ~15, q);
                         mma_commit(bar(kBarSfull + q));
                     }
                 }
@@ -374,7 +442,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             tc_fence_after();
                         }
                         if (leader) {
-                            issue_s(q, sk1, (nvalid1 + 15) & ~15);
+                            issue_s(q, sk1, (nvalid1 + 15) & ~15, q);
                             mma_commit(bar(kBarSfull + q));
                         }
                     }
@@ -394,29 +462,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
         const uint32_t tS = tmem + L::kTmemS + q * 128 + lane_off;
         const uint32_t tO = tmem + L::kTmemO + q * D + lane_off;
+        const uint32_t tO1 = tmem + L::kTmemO + D + lane_off;     // slot 1's O (alternating units)
         const float sc = p.scale_log2;
-        uint32_t it = 0, sq = 0, uq = 0, kc = 0;
+        float *xbuf = reinterpret_cast<float *>(smem + L::kX);
+        // uq: own slot's O-ready phases; uo1 (warpgroup 0): slot 1's; xc: row-sum handovers
+        uint32_t it = 0, sq = 0, uq = 0, kc = 0, uo1 = 0, xc = 0;
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
             decode(p, w, u);
-            const bool act = q < u.nact;
+            const bool act = q < u.nact || u.alt;
             // The last active warpgroup releases K, V and Q tiles: its S barrier for key
             // tile j is committed after every earlier MMA of the unit (all S MMAs of
             // tile j, all P.V MMAs of tile j-1); its O barrier covers the last P.V.
-            const bool releaser = q == u.nact - 1 && (warp % 4) == 0 && lane == 0;
+            const bool releaser = !u.alt && q == u.nact - 1 && (warp % 4) == 0 && lane == 0;
+            // alternating units: each warpgroup releases the K (and V two key tiles
+            // back) of its own key tiles
+            const bool rel_alt = u.alt && (warp % 4) == 0 && lane == 0;
             const uint32_t kc0 = kc;
             kc += u.nkt;
-            const bool stat =
-                p.mode == VDIT_MODE_FORCE_STATIC ||
-                (p.mode == VDIT_MODE_AUTO && (p.seg_elig ? p.seg_elig[(size_t)u.bh * p.nseg + u.seg]
-                                                          : p.elig[u.bh]) != 0);
+            const bool stat = u.stat;
             ok = mbar_wait_warp(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
             if (!ok) break;
             // row bound ("Unchaining the Softmax"): m~ = scale*log2e*(q.c + |q| R)
             float mt = 0.f;
             if (act && stat) {
-                const uint8_t *qt = smem + L::kQ + q * L::kTileBytes;
+                const uint8_t *qt = smem + L::kQ + (u.alt ? 0 : q) * L::kTileBytes;
                 const float *cm = p.k_mean + (size_t)u.bh * D;
                 float dot = 0.f, nn = 0.f;
 #pragma unroll
@@ -446,7 +517,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!act) continue;
 
             float l0 = 0.f, l1 = 0.f, mrun = -INFINITY;
-            for (int j = 0; j < u.nkt; ++j) {
+            for (int j = u.alt ? q : 0; j < u.nkt; j += u.alt ? 2 : 1) {
                 int start, nvalid;
                 key_tile(u, j, start, nvalid);
                 ok = mbar_wait_warp(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
@@ -455,6 +526,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (releaser) {
                     mbar_arrive(bar(kBarKfree + (kc0 + j) % kStagesK));
                     if (j > 0) mbar_arrive(bar(kBarVfree + (kc0 + j - 1) % kStagesV));
+                    if (j == u.nkt - 1) mbar_arrive(bar(kBarQfree));
+                }
+                if (rel_alt) {
+                    // S_q(j) was issued after P_q(j-2).V: K_j and V_{j-2} are free;
+                    // the last key tile's S is the unit's last S: Q is free
+                    mbar_arrive(bar(kBarKfree + (kc0 + j) % kStagesK));
+                    if (j >= 2) mbar_arrive(bar(kBarVfree + (kc0 + j - 2) % kStagesV));
                     if (j == u.nkt - 1) mbar_arrive(bar(kBarQfree));
                 }
                 float mrow = mt;
@@ -543,12 +621,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!stat) mt = mrun;
             }
             if (!ok) break;
+            float l = l0 + l1;
+            if (u.alt) {
+                // warpgroup 1 hands its row sums to warpgroup 0, which writes the tile
+                if (q == 1) {
+                    ok = mbar_wait_warp(bar(kBarXfree), (xc & 1) ^ 1, abort_flag, p.status, kSiteXfree, tlim);
+                    if (!ok) break;
+                    xbuf[r] = l;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kBarXfull));
+                    ++xc;
+                    ++uq;
+                    continue;
+                }
+                ok = mbar_wait_warp(bar(kBarXfull), xc & 1, abort_flag, p.status, kSiteXfull, tlim);
+                if (!ok) break;
+                l += xbuf[r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarXfree));
+                ++xc;
+                ok = mbar_wait_warp(bar(kBarOfull + 1), uo1 & 1, abort_flag, p.status, kSiteOfull, tlim);
+                if (!ok) break;
+            }
             ok = mbar_wait_warp(bar(kBarOfull + q), uq & 1, abort_flag, p.status, kSiteOfull, tlim);
             if (!ok) break;
             tc_fence_after();
             if (releaser) mbar_arrive(bar(kBarVfree + (kc0 + u.nkt - 1) % kStagesV));
-            // epilogue: O / l for the rows this tile owns, and LSE
-            const float l = l0 + l1;
+            if (rel_alt) {
+                mbar_arrive(bar(kBarVfree + (kc0 + u.nkt - 2) % kStagesV));
+                mbar_arrive(bar(kBarVfree + (kc0 + u.nkt - 1) % kStagesV));
+            }
+            // epilogue: O / l for the rows this tile owns, and LSE (alternating
+            // units: O = O0 + O1)
             const float inv = 1.0f / l;
             const int t = kTilesPerUnit * u.pair + q;
             const int row = tile_row(u, q) + r;
@@ -560,6 +664,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tO + c0, v);
+                if (u.alt) {
+                    uint32_t v1[32];
+                    tmem_ld32(tO1 + c0, v1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v1[e]));
+                }
                 if (owned) {
                     if (p.o_f32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + obase + c0);
@@ -587,8 +698,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 p.lse[((long long)u.bh * p.N) + row] = (mt + log2f(l)) * 0.69314718055994531f;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarOfree + q));
+            if (lane == 0) {
+                mbar_arrive(bar(kBarOfree + q));
+                if (u.alt) mbar_arrive(bar(kBarOfree + 1));
+            }
             ++uq;
+            if (q == 0 && (u.nact == 2 || u.alt)) ++uo1;
         }
     }
 
