@@ -99,10 +99,14 @@ struct Layout {
 
 // barrier slots (8 bytes each) after the tiles
 enum : int {
-    kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = 4, kBarVfull = 6, kBarVfree = 9,
-    kBarSfull = 12, kBarPfull = 14, kBarOfull = 16, kBarOfree = 18, kBarFinal = 20,
-    kBarXfull = 21, kBarXfree = 22, kNumBars = 23
+    kBarQfull = 0, kBarQfree = 1, kBarKfull = 2, kBarKfree = kBarKfull + kStagesK,
+    kBarVfull = kBarKfree + kStagesK, kBarVfree = kBarVfull + kStagesV,
+    kBarSfull = kBarVfree + kStagesV, kBarPfull = kBarSfull + 2, kBarOfull = kBarPfull + 2,
+    kBarOfree = kBarOfull + 2, kBarFinal = kBarOfree + 2,
+    kBarXfull = kBarFinal + 1, kBarXfree = kBarXfull + 1, kNumBars = kBarXfree + 1
 };
+// the barriers, the TMEM address word and the abort flag share the 256 bytes at kBar
+static_assert(8 * kNumBars + 8 <= 256, "barrier block overflows its 256 bytes");
 
 struct Params {
     const int32_t *segments, *units, *class_off;
