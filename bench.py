@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "effective TFLOP/s on live blocks, % of GB300 BF16 peak; ms per attention call"
 NOMINAL_BF16_TFLOPS = 2250.0
-FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 LAUNCHES_PER_STEP = 7   # plan meta + plan csr + stats pass1/mean/pass2/finalize + attention
 
 
@@ -68,6 +68,10 @@ def parse_args(argv=None):
                     help="instead of the one-line contract: time the attention call on every "
                          "workload and the dense eligibility sweep in AUTO, ONLINE and STATIC "
                          "modes, one JSON line per (workload, mode)")
+    ap.add_argument("--sustained", type=float, default=0.0, metavar="SECONDS",
+                    help="run the workload's attention call back to back for SECONDS under the "
+                         "board power limit and report its throughput with the clocks and power "
+                         "seen (one JSON line)")
     ap.add_argument("--traffic-bytes", type=float, default=None,
                     help="dram bytes per attention launch from an ncu capture (reported as is)")
     return ap.parse_args(argv)
@@ -78,8 +82,11 @@ def load_peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
-                "source": "measured"}
+        out = {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+               "source": "measured"}
+        if "bf16_tflops_sustained" in d:
+            out["bf16_tflops_sustained"] = float(d["bf16_tflops_sustained"])
+        return out
     except Exception:
         return dict(FALLBACK_PEAKS, source="fallback")
 
@@ -170,7 +177,7 @@ class ClockSampler:
         rows = [l.strip().split(", ") for l in self.tmp.read().splitlines() if l.strip()]
         self.tmp.close()
         os.unlink(self.tmp.name)
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             if len(r) < 9:
@@ -180,13 +187,20 @@ class ClockSampler:
                 mx = float(r[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(r[3]))
+            except ValueError:
+                pass
             for n, val in zip(names, r[5:9]):
                 if val.strip().lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if pw:
+            out["power_w"] = statistics.median(pw)
+        return out
 
 
 def live_pairs_of_rows(w, rows, frame_runs):
@@ -490,6 +504,58 @@ def run_pipeline_sweep(args):
     return 0
 
 
+def run_sustained(args):
+    """The attention call repeated back to back for a few seconds: a dense
+    contraction at this rate holds the board at its power limit, and the SM
+    clock settles below its maximum. Reports the settled throughput, the
+    clocks and power sampled over the run (the first and last half second are
+    dropped), and the fraction of the measured sustained bf16 GEMM rate."""
+    import torch
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+    torch.cuda.set_device(0)
+    vd.load_library()
+    w = configs.BY_NAME[args.workload]
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    st = vd.key_stats(q, k, w.scale)
+    o, lse = vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    burst = 20
+    # settle under the power limit first, then time while sampling
+    t0 = time.time()
+    while time.time() - t0 < 0.5 * args.sustained:
+        for _ in range(burst):
+            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode)
+        torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 0
+    t0 = time.time()
+    a.record(stream)
+    while time.time() - t0 < args.sustained:
+        for _ in range(burst):
+            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode)
+        n += burst
+        torch.cuda.synchronize()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if plan.status() != 0:
+        raise RuntimeError("an attention wait expired")
+    ms = a.elapsed_time(b) / n
+    tflops = 4.0 * w.D * plan.live_pairs * w.B * w.H / (ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    sus = peaks.get("bf16_tflops_sustained") if peaks else None
+    print(json.dumps({"workload": w.name, "mode": args.mode, "calls": n, "seconds": args.sustained,
+                      "ms_per_call": ms, "tflops": tflops, "clocks": clk,
+                      "frac_of_sustained_bf16": tflops / sus if sus else None,
+                      "sustained_bf16_tflops": sus}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -502,6 +568,8 @@ def main(argv=None):
         return run_pipeline_sweep(args)
     if args.bs_sweep:
         return run_bs_sweep(args)
+    if args.sustained > 0:
+        return run_sustained(args)
 
     import torch
     import torch.distributed as dist
