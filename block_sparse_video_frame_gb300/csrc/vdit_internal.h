@@ -39,6 +39,7 @@ constexpr int kTilesPerUnit = 2; // query tiles that share one K/V stream
 constexpr int kSegInts = 8;      // ints per segment record
 constexpr int kMaxFrames = 4096; // frames a plan may hold
 constexpr int kMaxClasses = 64;  // distinct unit costs a plan may hold
+constexpr int kMaxPairsPerSegment = 1 << 16;  // tile pairs a segment may hold (16-bit field)
 
 // Header the schedule kernel writes (device), read back once by the host.
 struct PlanHeader {

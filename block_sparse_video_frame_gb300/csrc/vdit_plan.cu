@@ -113,7 +113,10 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_run
         int32_t *g = segments + kSegInts * s;
         g[6] = (g[1] + kTileRows - 1) / kTileRows;
         s_order[s] = s;
+        // a unit code keeps the tile pair in its low 16 bits
+        if ((g[6] + kTilesPerUnit - 1) / kTilesPerUnit > kMaxPairsPerSegment) h.error = 4;
     }
+    if (h.error != 0) nseg = 0;
     // longest first (stable insertion sort on key count) ------------------
     for (int i = 1; i < nseg; ++i) {
         int v = s_order[i], key = segments[kSegInts * v + 7], j = i - 1;
@@ -273,6 +276,14 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
         free_plan_buffers(p);
         delete p;
         return cuda_fail(e, "vdit_attn_plan: schedule kernel");
+    }
+    if (p->h.error == 4) {
+        set_error("vdit_attn_plan: a run of frames with equal key runs holds more than %d query rows "
+                  "(%d tile pairs), beyond the work-unit encoding",
+                  kMaxPairsPerSegment * kTileRows * kTilesPerUnit, kMaxPairsPerSegment);
+        free_plan_buffers(p);
+        delete p;
+        return VDIT_ERR_UNSUPPORTED;
     }
     if (p->h.error != 0 || p->h.nnz >= (1ll << 31)) {
         set_error("vdit_attn_plan: schedule too large (error %d, nnz %lld)", p->h.error, p->h.nnz);

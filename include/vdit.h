@@ -89,8 +89,11 @@ typedef struct {
  *   (W >= F-1), where a ragged last block is allowed. F*T < 2^31.
  * Allocates the plan's device buffers, launches the schedule kernels on
  * `stream`, and synchronises once to read the counts. *out receives the plan
- * (NULL on error). Errors: VDIT_ERR_INVALID (argument), VDIT_ERR_NOMEM,
- * VDIT_ERR_CUDA. */
+ * (NULL on error). Errors: VDIT_ERR_INVALID (argument, or a CSR with 2^31 or
+ * more live blocks), VDIT_ERR_UNSUPPORTED (a segment -- consecutive frames
+ * sharing one key-run list, the whole sequence when dense -- of more than
+ * 2^24 query rows: its 128-row tile pairs would not fit the 16-bit pair field
+ * of d_units), VDIT_ERR_NOMEM, VDIT_ERR_CUDA. */
 VDIT_API vdit_status vdit_attn_plan(int32_t num_frames, int32_t tokens_per_frame, int32_t window_radius,
                            int32_t ref_frame, int32_t block_size, void *stream, vdit_plan **out);
 

@@ -67,3 +67,22 @@ def test_work_units_cover_every_query_tile_once(F, T, W, ref, bs):
     assert cls[0] == 0 and cls[-1] == len(units)
     for a, b in zip(cls[:-1], cls[1:]):
         assert len(set(keys[a:b])) == 1
+
+
+def test_segment_at_the_tile_pair_field_limit():
+    """Maximum size of the work-unit encoding (segment << 16 | tile pair): a
+    dense sequence of exactly 2^24 rows fills the 16-bit pair field with 65 536
+    pairs; one more 128-row tile is refused as unsupported instead of wrapping
+    into the segment field."""
+    T = 1 << 24
+    plan = vd.attn_plan(1, T, 0, 0, 4096)
+    units = plan.units().cpu().numpy().astype(np.int64)
+    assert plan.info.n_segments == 1 and len(units) == 65536
+    assert (units >> 16 == 0).all()
+    assert np.array_equal(units & 0xFFFF, np.arange(65536))
+    assert plan.info.live_pairs == T * T
+    plan.close()
+    with pytest.raises(vd.VditError) as ei:
+        vd.attn_plan(1, T + 128, 0, 0, 4096)
+    assert ei.value.status == vd.VDIT_ERR_UNSUPPORTED
+    assert "tile pairs" in str(ei.value)
