@@ -14,6 +14,12 @@ Parity pins (tests/test_oracle_*.py): closed-form schedule counts, brute force
 on tiny inputs, dense and block-diagonal special cases against torch's float64
 scaled-dot-product attention, centring and permutation invariance, bound >= max,
 key statistics against numpy. No function is "parity unpinned".
+tests/test_oracle_mutants.py plants mistakes in copies of the C source and
+checks that these pins reject every one.
+
+VDIT_ORACLE_LIB, when set, names an already built oracle library to load
+instead of building ``vdit_oracle.c`` (the planted-mistake tests point it at
+their mutated builds).
 """
 from __future__ import annotations
 
@@ -37,14 +43,21 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
+GCC_FLAGS = ("-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11")
+
+
+def compile_source(src: str, out: str) -> None:
+    """gcc one oracle source file into a shared library (fp64, no fast-math, no
+    FMA contraction)."""
+    subprocess.run(["gcc", *GCC_FLAGS, "-o", out, src, "-lm"], check=True)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (fp64, no fast-math, no FMA contraction)."""
+    """Compile the oracle (vdit_oracle.c) into oracle/_build/liboracle.so."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-               "-std=c11", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_source(_SRC, tmp)
         os.replace(tmp, _SO)
     return _SO
 
@@ -54,7 +67,7 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        lib = ctypes.CDLL(os.environ.get("VDIT_ORACLE_LIB") or build())
         lib.vo_set_threads.argtypes = [ctypes.c_int]
         lib.vo_set_threads.restype = ctypes.c_int
         lib.vo_mask.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,

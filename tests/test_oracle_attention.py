@@ -148,6 +148,33 @@ def test_bound_is_tight_for_aligned_key():
     np.testing.assert_allclose(mx, [3.0, 3.0], atol=1e-15)
 
 
+def test_bound_closed_form_with_offset_mean():
+    """Closed form with a non-zero key mean c: keys c +- a e0 and c +- a e1 have
+    mean c and R = a. A query along e0 meets the Cauchy-Schwarz equality case, so
+    its bound scale*(q.c + |q| a) equals its true max; a query along e2 sees the
+    same logit scale*q.c on every key, so its bound exceeds its max by exactly
+    scale*|q|*a. Both the q.c term and the |q| R term are needed to match."""
+    D, a, scale = 8, 2.0, 0.5
+    c = np.zeros(D); c[:3] = [1.5, -0.75, 0.5]
+    k = np.tile(c, (1, 1, 4, 1))
+    k[0, 0, 0, 0] += a; k[0, 0, 1, 0] -= a; k[0, 0, 2, 1] += a; k[0, 0, 3, 1] -= a
+    q = np.zeros((1, 1, 4, D)); q[0, 0, 0, 0] = 2.0; q[0, 0, 1, 2] = 3.0
+    q[0, 0, 2, 0] = -1.0; q[0, 0, 3, 1] = 0.5
+    v = rand64((1, 1, 4, D), 2)
+    st = oracle.key_stats(q, k, scale, 64.0)
+    np.testing.assert_allclose(st["c"].reshape(-1), c, atol=0, rtol=0)
+    assert st["R"][0, 0] == a
+    m = oracle.row_bounds(q, st["c"], st["R"], scale)
+    _, _, mx = oracle.attention_rows(q, k, v, 4, 0, -1, scale)   # one frame of 4 tokens
+    qc = q[0, 0] @ c
+    qn = np.linalg.norm(q[0, 0], axis=-1)
+    np.testing.assert_allclose(m, scale * (qc + qn * a), atol=1e-15, rtol=0)
+    # rows 0, 2, 3 point along a key axis (equality case); row 1 is orthogonal to both
+    np.testing.assert_allclose(mx[[0, 2, 3]], m[[0, 2, 3]], atol=1e-15, rtol=0)
+    assert mx[1] == pytest.approx(scale * qc[1], abs=1e-15)
+    assert m[1] - mx[1] == pytest.approx(scale * 3.0 * a, abs=1e-15)
+
+
 def test_static_max_equals_max_subtracted():
     """Softmax with the precomputed bound as the shift equals the ordinary
     max-subtracted softmax (the static-max reformulation is exact)."""
