@@ -139,18 +139,30 @@ struct Work {
     bool alt;              // lone static tile: slots 0 and 1 take alternate key tiles
 };
 
+// Work order. CTA b takes work items b, b + grid, b + 2*grid, ... The items walk
+// the heads in groups of kHeadGroup. Inside a group they walk the plan's cost
+// classes longest first, and inside a class every head of the group with its
+// units. So the CTAs running at one time share the K/V of at most a few heads,
+// which stay in L2 (24 MB per head at 720p, D = 128). A head-major walk would
+// still revisit each head's K/V once per cost class, after it has left L2.
+constexpr int kHeadGroup = 2;
+
 __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
     const int BH = p.B * p.H;
+    const long long per_head = p.class_off[p.n_classes];
+    const long long g = w / (per_head * kHeadGroup);
+    const int gh = min(kHeadGroup, BH - (int)g * kHeadGroup);   // heads in this group
+    w -= g * per_head * kHeadGroup;
     long long base = 0;
     int c = 0, n_c = 0;
     for (c = 0; c < p.n_classes; ++c) {
         n_c = p.class_off[c + 1] - p.class_off[c];
-        const long long span = (long long)n_c * BH;
+        const long long span = (long long)n_c * gh;
         if (w < base + span) break;
         base += span;
     }
     const long long local = w - base;
-    u.bh = (int)(local / n_c);
+    u.bh = (int)(g * kHeadGroup + local / n_c);
     const int ui = p.class_off[c] + (int)(local % n_c);
     u.b = u.bh / p.H;
     u.h = u.bh % p.H;
