@@ -106,4 +106,7 @@ PRO_TINY = PrologueShape("pro_tiny", B=1, N=200, C=128, H=2, D=64)           # r
 PRO_RAGGED = PrologueShape("pro_ragged", B=2, N=300, C=200, H=3, D=128, seed=1)  # K tail, half column tile
 PRO_SMALL = PrologueShape("pro_small", B=1, N=3600, C=1024, H=8, D=128, seed=2)
 PRO_SR720 = PrologueShape("pro_sr720p", B=1, N=46800, C=3072, H=24, D=128, seed=3)
+# W' of 35 MB: the GEMM walks its column tiles in two bands (23 tiles: 12 + 11, the
+# last one half wide) over 700 ragged rows
+PRO_BANDS = PrologueShape("pro_bands", B=1, N=700, C=3072, H=15, D=128, seed=4)
 PROLOGUE = (PRO_TINY, PRO_RAGGED, PRO_SMALL, PRO_SR720)

@@ -235,6 +235,7 @@ enum : int { kSiteEmpty = 101, kSiteFull, kSiteAccEmpty, kSiteAccFull };
 struct GemmParams {
     int B, N, H, D, C, O;        // O = 3 H D output columns
     int pairs_m, tiles_n, kb;    // 256-row blocks per batch, column tiles, K stages per tile
+    int col_bands;               // column bands the tiles are walked in (see tile_of)
     long long total;             // B * pairs_m * tiles_n pair tiles
     const float *inv_rms;        // [B * N]
     const float2 *rope;          // [D/2][N] (cos, sin)
@@ -323,13 +324,21 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
 struct TileId {
     int b, mp, nt;
 };
+// Tile order. The output columns are walked in p.col_bands bands. Inside a band the
+// column tiles go fastest, so concurrent pairs share x rows, and every 256-row block
+// is visited before the next band starts. So only one band of W' has to stay in L2
+// while x and the outputs stream through it, at the price of reading x once per band.
 __device__ __forceinline__ TileId tile_of(const GemmParams &p, long long t) {
     const long long per_b = (long long)p.pairs_m * p.tiles_n;
     TileId id;
     id.b = (int)(t / per_b);
     const int rem = (int)(t - (long long)id.b * per_b);
-    id.mp = rem / p.tiles_n;     // column tiles fastest: concurrent pairs share x rows
-    id.nt = rem % p.tiles_n;
+    const int nb = (p.tiles_n + p.col_bands - 1) / p.col_bands;   // tiles per full band
+    const int band = rem / (p.pairs_m * nb);
+    const int r2 = rem - band * p.pairs_m * nb;
+    const int wb = min(nb, p.tiles_n - band * nb);                // this band's width
+    id.mp = r2 / wb;
+    id.nt = band * nb + r2 % wb;
     return id;
 }
 
@@ -800,6 +809,15 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
     prm.tiles_n = (int)((O + kBN - 1) / kBN);
     prm.kb = (C + kBK - 1) / kBK;
     prm.total = (long long)B * prm.pairs_m * prm.tiles_n;
+    {
+        // one band per 24 MB of W' (three for the 9216 x 3072 projection): a band of W'
+        // then stays in L2 beside the streaming x and outputs. DRAM reads at that
+        // size: 1.83 GB in one band, 1.34 GB in two, 1.06 GB in three.
+        const long long w_bytes = O * (long long)C * 2;
+        const long long band_bytes = 24ll << 20;
+        const long long bands = (w_bytes + band_bytes - 1) / band_bytes;
+        prm.col_bands = (int)(bands < 1 ? 1 : (bands > prm.tiles_n ? prm.tiles_n : bands));
+    }
     prm.inv_rms = inv_rms;
     prm.rope = reinterpret_cast<const float2 *>(rope);
     prm.status = reinterpret_cast<int *>(wsb);

@@ -116,6 +116,20 @@ def test_prologue_all_rows_exact_gain(s):
     check(s, got, ref, rows)
 
 
+def test_prologue_column_bands_all_rows():
+    """A projection large enough that the GEMM walks its output columns in two
+    bands (one per 24 MB of W'), with an uneven last band and a half-wide last
+    column tile: every row against the oracle."""
+    s = configs.PRO_BANDS
+    assert -(-s.O * s.C * 2 // (24 << 20)) == 2      # the band rule of the library
+    x, w, gamma = synth.make_prologue_inputs(s.B, s.N, s.C, s.H, s.D, s.seed, exact_gain=True)
+    got = run_gpu(s, x, w, gamma)
+    torch.cuda.synchronize()
+    rows = np.arange(s.B * s.N, dtype=np.int64)
+    ref = oracle.qkv_prologue(x, w, gamma.double().numpy(), s.H, s.D, s.eps, s.base, rows)
+    check(s, got, ref, rows)
+
+
 def test_prologue_general_gain():
     s = configs.PRO_RAGGED
     x, w, gamma = synth.make_prologue_inputs(s.B, s.N, s.C, s.H, s.D, s.seed + 10)
