@@ -835,7 +835,7 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
         set_error("vdit_attn_fwd: eligible is required in AUTO mode");
         return VDIT_ERR_INVALID;
     }
-    if (!(scale > 0.f)) { set_error("vdit_attn_fwd: scale must be > 0"); return VDIT_ERR_INVALID; }
+    if (!finite_positive(scale)) { set_error("vdit_attn_fwd: scale must be finite and > 0"); return VDIT_ERR_INVALID; }
     const int64_t *sts[3] = {q_strides, k_strides, v_strides};
     for (int t = 0; t < 3; ++t)
         for (int i = 0; i < 3; ++i)

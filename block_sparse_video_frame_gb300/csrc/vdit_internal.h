@@ -41,6 +41,9 @@ constexpr int kMaxFrames = 4096; // frames a plan may hold
 constexpr int kMaxClasses = 64;  // distinct unit costs a plan may hold
 constexpr int kMaxPairsPerSegment = 1 << 16;  // tile pairs a segment may hold (16-bit field)
 
+// A scale factor the kernels can use: positive and finite (NaN and +inf fail).
+inline bool finite_positive(float x) { return x > 0.f && x <= 3.402823466e38f; }
+
 // Header the schedule kernel writes (device), read back once by the host.
 struct PlanHeader {
     long long nnz;

@@ -292,8 +292,8 @@ extern "C" vdit_status vdit_key_stats(const void *q, const void *k, int32_t B, i
         set_error("vdit_key_stats: workspace of %zu bytes < %zu needed", workspace_bytes, need);
         return VDIT_ERR_INVALID;
     }
-    if (!(scale > 0.f) || !(tau >= 0.f)) {
-        set_error("vdit_key_stats: scale must be > 0 and tau >= 0");
+    if (!finite_positive(scale) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats: scale must be finite and > 0, tau >= 0");
         return VDIT_ERR_INVALID;
     }
     StatsArgs a;
@@ -399,8 +399,8 @@ extern "C" vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int3
         set_error("vdit_key_stats_noalloc: q and k must be 16-byte aligned");
         return VDIT_ERR_INVALID;
     }
-    if (!(scale > 0.f) || !(tau >= 0.f)) {
-        set_error("vdit_key_stats_noalloc: scale must be > 0 and tau >= 0");
+    if (!finite_positive(scale) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats_noalloc: scale must be finite and > 0, tau >= 0");
         return VDIT_ERR_INVALID;
     }
     const size_t need = vdit_key_stats_workspace_size(B, H, N, D);
@@ -487,8 +487,8 @@ extern "C" vdit_status vdit_key_stats_framed(const vdit_plan *plan, const void *
         set_error("vdit_key_stats_framed: workspace of %zu bytes < %zu needed", workspace_bytes, need);
         return VDIT_ERR_INVALID;
     }
-    if (!(scale > 0.f) || !(tau >= 0.f)) {
-        set_error("vdit_key_stats_framed: scale must be > 0 and tau >= 0");
+    if (!finite_positive(scale) || !(tau >= 0.f)) {
+        set_error("vdit_key_stats_framed: scale must be finite and > 0, tau >= 0");
         return VDIT_ERR_INVALID;
     }
     int dev = -1;

@@ -125,7 +125,8 @@ VDIT_API size_t vdit_key_stats_workspace_size(int32_t B, int32_t H, int32_t N, i
  *   eligible[b,h]  = (G <= tau) ? 1 : 0                          uint8 [B, H]
  * G bounds, for every row and every mask, how far the row's static bound can
  * sit above its true max logit; tau = 64 keeps every row's largest term above
- * e^-64, far from fp32 underflow. q, k: bf16 device tensors (see conventions).
+ * e^-64, far from fp32 underflow. scale: finite and > 0; tau >= 0 (+inf makes
+ * every head eligible). q, k: bf16 device tensors (see conventions).
  * workspace: device buffer of at least vdit_key_stats_workspace_size bytes,
  * caller-owned, contents need not be initialised. Reductions run in a fixed
  * order: results are bitwise reproducible. Outputs are dense, caller-owned
@@ -167,6 +168,8 @@ VDIT_API vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int32_
  * and online softmax elsewhere; FORCE_ONLINE uses online softmax everywhere
  * (k_mean, k_rmax, eligible may be NULL); FORCE_STATIC uses the bound on every
  * head (eligible may be NULL; on ineligible heads terms may underflow).
+ * scale: finite and > 0. o and lse must not share memory with q, k or v (the
+ * kernel reads q, k, v tiles while other CTAs write o).
  * k_mean, k_rmax: outputs of vdit_key_stats for the same k. A kernel whose
  * bounded wait expires stops early and sets the plan's status word (see
  * vdit_plan_status). The result is deterministic: two identical calls write

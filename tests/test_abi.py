@@ -81,6 +81,13 @@ def test_key_stats_rejects_bad_arguments(lib):
     assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
     bad = list(args); bad[6] = vd._I64x3(8 * 128, 128 * 16, 100)
     assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+    for scale in (0.0, -0.1, float("inf"), float("nan")):
+        bad = list(args); bad[8] = scale
+        assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
+        assert "scale" in lib.vdit_last_error().decode()
+    for tau in (-1.0, float("nan")):
+        bad = list(args); bad[9] = tau
+        assert lib.vdit_key_stats(*bad) == vd.VDIT_ERR_INVALID
 
 
 def test_attn_fwd_rejects_null_plan(lib):

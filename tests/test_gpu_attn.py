@@ -146,3 +146,14 @@ def test_full_size_sampled_rows(w):
     assert torch.equal(o16, o32.to(torch.bfloat16))
     # properties that hold at any size: every row finite; LSE finite
     assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
+
+
+def test_non_finite_scale_is_rejected():
+    w = configs.TINY
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    st = vd.key_stats(q, k, w.scale)
+    for scale in (float("inf"), float("nan"), 0.0):
+        with pytest.raises(vd.VditError) as ei:
+            vd.attn_fwd(plan, q, k, v, st, scale)
+        assert ei.value.status == vd.VDIT_ERR_INVALID and "scale" in str(ei.value)
