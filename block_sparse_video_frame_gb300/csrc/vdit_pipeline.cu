@@ -285,6 +285,15 @@ extern "C" vdit_status vdit_pipeline_run(vdit_pipeline *p, const void *q_host, c
         set_error("vdit_pipeline_run: host token stride is below D");
         return VDIT_ERR_INVALID;
     }
+    // checked here too, before any copy is queued (the per-group calls repeat them)
+    if (!finite_positive(scale) || !(tau >= 0.f)) {
+        set_error("vdit_pipeline_run: scale must be finite and > 0, tau >= 0");
+        return VDIT_ERR_INVALID;
+    }
+    if (mode < VDIT_MODE_AUTO || mode > VDIT_MODE_FORCE_STATIC) {
+        set_error("vdit_pipeline_run: mode=%d invalid", mode);
+        return VDIT_ERR_INVALID;
+    }
     int dev = -1;
     VDIT_CUDA_TRY(cudaGetDevice(&dev));
     if (dev != p->device) {

@@ -331,7 +331,11 @@ VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int3
  * respect to the host: the work is ordered after everything already queued on
  * `stream`, and `stream` waits for all of it, so a synchronisation of `stream`
  * means o_host (and lse_host) are complete. An expired wait inside attention
- * is reported by vdit_plan_status on the plan. Errors: VDIT_ERR_INVALID,
+ * is reported by vdit_plan_status on the plan. Arguments (pointers, strides,
+ * scale finite and > 0, tau >= 0, mode) are checked before anything is queued.
+ * An error from a later step returns at once; copies and kernels of earlier
+ * groups may still be in flight, and the host buffers must stay valid until
+ * `stream` (or the device) is synchronised. Errors: VDIT_ERR_INVALID,
  * VDIT_ERR_CUDA, and those of vdit_key_stats and vdit_attn_fwd. */
 VDIT_API vdit_status vdit_pipeline_run(vdit_pipeline *pipeline, const void *q_host,
                                        const void *k_host, const void *v_host, void *o_host,

@@ -115,3 +115,24 @@ def test_pipeline_batches_and_head_dim_64(w, groups):
     assert plan.status() == 0
     assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
     assert torch.equal(lse_h, lse_ref)
+
+
+def test_pipeline_rejects_bad_scalars_before_queuing():
+    w = configs.TINY
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+    o_h = pinned_like(q)
+    o_h.fill_(3.0)
+    pipe = vd.Pipeline(plan, w.B, w.H, w.D, 2)
+    for scale in (float("inf"), float("nan"), -1.0):
+        with pytest.raises(vd.VditError) as ei:
+            pipe.run(q_h, k_h, v_h, o_h, scale)
+        assert ei.value.status == vd.VDIT_ERR_INVALID and "scale" in str(ei.value)
+    torch.cuda.synchronize()
+    assert bool((o_h == 3.0).all()), "a rejected call must not write the output"
+    pipe.run(q_h, k_h, v_h, o_h, w.scale)          # the pipeline stays usable
+    torch.cuda.synchronize()
+    o_ref, _ = device_reference(w, q, k, v, plan)
+    assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
+    pipe.close()
