@@ -698,7 +698,7 @@ extern "C" vdit_status vdit_rope_table(float *table, int32_t N, int32_t D, doubl
         set_error("vdit_rope_table: N=%d must be >= 1 and D=%d even and >= 2", N, D);
         return VDIT_ERR_INVALID;
     }
-    if (!(base > 0.0)) { set_error("vdit_rope_table: base must be > 0"); return VDIT_ERR_INVALID; }
+    if (!(base > 0.0 && base <= 1.7976931348623157e308)) { set_error("vdit_rope_table: base must be finite and > 0"); return VDIT_ERR_INVALID; }
     if (reinterpret_cast<uintptr_t>(table) & 7u) {
         set_error("vdit_rope_table: table must be 8-byte aligned");
         return VDIT_ERR_INVALID;
@@ -739,7 +739,7 @@ extern "C" vdit_status vdit_qkv_prologue(const void *x, const int64_t x_strides[
     if (C % 8 != 0) { set_error("vdit_qkv_prologue: C=%d must be a multiple of 8", C); return VDIT_ERR_INVALID; }
     const long long O = 3ll * H * D;
     if (O > (1ll << 30)) { set_error("vdit_qkv_prologue: 3*H*D too large"); return VDIT_ERR_INVALID; }
-    if (!(eps >= 0.f)) { set_error("vdit_qkv_prologue: eps must be >= 0"); return VDIT_ERR_INVALID; }
+    if (!(eps >= 0.f && eps <= 3.402823466e38f)) { set_error("vdit_qkv_prologue: eps must be finite and >= 0"); return VDIT_ERR_INVALID; }
     for (int i = 0; i < 2; ++i)
         if (x_strides[i] <= 0 || x_strides[i] % 8 != 0 || x_strides[i] >= (1ll << 38)) {
             set_error("vdit_qkv_prologue: x strides must be positive multiples of 8 elements");

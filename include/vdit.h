@@ -258,7 +258,7 @@ VDIT_API vdit_status vdit_qkv_fold_gamma(const void *w, const float *gamma, void
  * that consecutive rows read consecutive entries). Any other angle schedule
  * (e.g. per-axis angles for frame, height and width) may be written into the
  * same layout by the caller. Errors: VDIT_ERR_INVALID (null table, N < 1,
- * D odd or < 2, base <= 0), VDIT_ERR_CUDA. */
+ * D odd or < 2, base not finite and > 0), VDIT_ERR_CUDA. */
 VDIT_API vdit_status vdit_rope_table(float *table, int32_t N, int32_t D, double base, void *stream);
 
 /* Bytes of device workspace vdit_qkv_prologue needs: one status word and one
@@ -270,7 +270,7 @@ VDIT_API size_t vdit_qkv_workspace_size(int32_t B, int32_t N);
  *   w_folded: bf16 [3*H*D, C] dense, the output of vdit_qkv_fold_gamma
  *   rope:     fp32 [D/2][N][2] angle table (see vdit_rope_table)
  *   q, k, v:  bf16 [B, H, N, D] outputs, strides in elements for (b, h, n)
- *   eps:      RMSNorm epsilon (>= 0)
+ *   eps:      RMSNorm epsilon (finite, >= 0)
  *   workspace: >= vdit_qkv_workspace_size(B, N) bytes of device memory; its
  *             status word must be zero at launch (it is after a fresh cudaMemset
  *             and after vdit_qkv_status).

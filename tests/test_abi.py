@@ -140,4 +140,9 @@ def test_prologue_entry_points_reject_bad_arguments(lib):
     assert lib.vdit_qkv_workspace_size(1, 46800) >= 46800 * 4
     assert lib.vdit_rope_table(None, 16, 128, 1e4, None) == vd.VDIT_ERR_INVALID
     assert lib.vdit_rope_table(p, 16, 127, 1e4, None) == vd.VDIT_ERR_INVALID
+    for base in (0.0, float("inf"), float("nan")):
+        assert lib.vdit_rope_table(p, 16, 128, base, None) == vd.VDIT_ERR_INVALID
+    for eps in (-1e-6, float("inf"), float("nan")):
+        st = lib.vdit_qkv_prologue(p, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1024, 8, 128, eps, p, 1 << 20, None)
+        assert st == vd.VDIT_ERR_INVALID and "eps" in lib.vdit_last_error().decode()
     assert lib.vdit_qkv_fold_gamma(None, p, p, 4, 8, None) == vd.VDIT_ERR_INVALID
