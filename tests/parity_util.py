@@ -14,18 +14,22 @@ LSE_ABS = 1e-3
 
 def stratified_rows(w, per_frame_random=13, seed=1234):
     """Flattened row indices ((b*H + h)*N + i): per (b, h, frame) the frame's
-    first and last row, the first row of its last 128-row tile (shifted to end
-    at the frame end), and `per_frame_random` seeded uniform rows."""
+    first and last row and `per_frame_random` seeded uniform rows; per segment
+    (rows sharing one key-run list: a frame, or the whole sequence when dense)
+    the first row of its last 128-row tile, which is shifted to end at the
+    segment's end."""
     rng = np.random.default_rng(seed)
     rows = []
-    seg = w.N if w.dense else w.T            # rows sharing one key-run list
-    nseg = w.N // seg
+    seg = w.N if w.dense else w.T
     for bh in range(w.B * w.H):
-        for s in range(nseg):
-            lo, hi = s * seg, (s + 1) * seg
-            picks = {lo, hi - 1, max(lo, hi - 128)}
+        picks = set()
+        for f in range(w.F):
+            lo, hi = f * w.T, (f + 1) * w.T
+            picks.update((lo, hi - 1))
             picks.update(int(x) for x in rng.integers(lo, hi, per_frame_random))
-            rows.extend(bh * w.N + i for i in sorted(picks))
+        for s0 in range(0, w.N, seg):
+            picks.add(max(s0, s0 + seg - 128))
+        rows.extend(bh * w.N + i for i in sorted(picks))
     return np.array(rows, dtype=np.int64)
 
 

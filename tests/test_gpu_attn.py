@@ -157,3 +157,31 @@ def test_non_finite_scale_is_rejected():
         with pytest.raises(vd.VditError) as ei:
             vd.attn_fwd(plan, q, k, v, st, scale)
         assert ei.value.status == vd.VDIT_ERR_INVALID and "scale" in str(ei.value)
+
+
+def _full_size_check(w, mode, per_frame_random):
+    q, k, v = synth.make_qkv(w)
+    rows = stratified_rows(w, per_frame_random=per_frame_random)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v, rows)
+    o32, lse, st, plan = run_gpu(w, q, k, v, mode=mode)
+    check_close(gather_rows(o32, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref,
+                f"{w.name} {mode}")
+    assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
+    return st
+
+
+def test_full_size_forced_online_720p():
+    """The online-softmax path (running max, lazy rescale of O) over the 720p-like
+    workload's ~150 key tiles per unit, on every head."""
+    _full_size_check(configs.SR720, "online", per_frame_random=4)
+
+
+def test_full_size_dense_sweep_large_key_offset():
+    """Dense sweep point with key offsets of scale 2 and 6 outlier heads: the
+    mean term q.c of the bound is large (centring keeps the 18 regular heads
+    eligible, the outliers take the online path), over a key count that is not
+    a multiple of 16."""
+    w = {x.name: x for x in configs.dense_sweep()}["dense_s2_out6"]
+    st = _full_size_check(w, "auto", per_frame_random=3)
+    elig = st["eligible"].cpu().numpy().reshape(-1)
+    assert elig[:18].all() and not elig[18:].any()
