@@ -36,7 +36,8 @@ struct Slot {
     uint8_t *elig = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
-    cudaEvent_t in_ready = nullptr, computed = nullptr, out_done = nullptr;
+    // qk_ready: q and k landed (the key statistics may start); in_ready: v too
+    cudaEvent_t qk_ready = nullptr, in_ready = nullptr, computed = nullptr, out_done = nullptr;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -79,6 +80,7 @@ namespace {
 void release(vdit_pipeline *p) {
     if (!p) return;
     for (Slot &s : p->slot) {
+        if (s.qk_ready) cudaEventDestroy(s.qk_ready);
         if (s.in_ready) cudaEventDestroy(s.in_ready);
         if (s.computed) cudaEventDestroy(s.computed);
         if (s.out_done) cudaEventDestroy(s.out_done);
@@ -247,7 +249,7 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
         s.gap = reinterpret_cast<float *>(m); m += align_up((size_t)B * hg * 4);
         s.elig = m; m += align_up((size_t)B * hg);
         s.ws = m; s.ws_bytes = ws_bytes;
-        for (cudaEvent_t *ev : {&s.in_ready, &s.computed, &s.out_done}) {
+        for (cudaEvent_t *ev : {&s.qk_ready, &s.in_ready, &s.computed, &s.out_done}) {
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) {
                 release(p);
                 return cuda_fail(e, "vdit_pipeline_create: cudaEventCreate");
@@ -316,17 +318,21 @@ extern "C" vdit_status vdit_pipeline_run(vdit_pipeline *p, const void *q_host, c
         if (reuse) VDIT_CUDA_TRY(cudaStreamWaitEvent(p->s_in, s.computed, 0));
         const void *ins[3] = {q_host, k_host, v_host};
         uint8_t *dsts[3] = {s.q, s.k, s.v};
-        for (int t = 0; t < 3; ++t)
+        for (int t = 0; t < 3; ++t) {
             VDIT_CUDA_TRY(copy_group(dsts[t], static_cast<uint8_t *>(const_cast<void *>(ins[t])), host_strides, B,
                                      N, D, h0, hc, 2, cudaMemcpyHostToDevice, p->s_in));
+            if (t == 1) VDIT_CUDA_TRY(cudaEventRecord(s.qk_ready, p->s_in));
+        }
         VDIT_CUDA_TRY(cudaEventRecord(s.in_ready, p->s_in));
-        // kernels: the slot's O is free once group g - 2's copy-out finished
-        VDIT_CUDA_TRY(cudaStreamWaitEvent(s_cmp, s.in_ready, 0));
+        // kernels: the slot's O is free once group g - 2's copy-out finished. The key
+        // statistics read only q and k, so they start while v is still copying.
+        VDIT_CUDA_TRY(cudaStreamWaitEvent(s_cmp, s.qk_ready, 0));
         if (reuse) VDIT_CUDA_TRY(cudaStreamWaitEvent(s_cmp, s.out_done, 0));
         vdit_status st = vdit_key_stats(s.q, s.k, B, hc, N, D, L.dev_strides, L.dev_strides, scale, tau,
                                         s.k_mean, s.k_rmax, s.q_nmax, s.gap, s.elig, s.ws, s.ws_bytes,
                                         s_cmp);
         if (st != VDIT_OK) return st;
+        VDIT_CUDA_TRY(cudaStreamWaitEvent(s_cmp, s.in_ready, 0));
         st = vdit_attn_fwd(p->plan, s.q, s.k, s.v, s.o, VDIT_O_BF16, lse_host ? s.lse : nullptr, B, hc, D,
                            L.dev_strides, L.dev_strides, L.dev_strides, L.dev_strides, scale, s.k_mean,
                            s.k_rmax, s.elig, mode, s_cmp);
