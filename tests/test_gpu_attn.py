@@ -36,6 +36,7 @@ SMALL_CASES = [
                      outlier_heads=(1,), seed=15),
     configs.Workload("wide_w", B=1, H=2, D=64, F=10, T=64, W=3, ref=0, block_size=64,
                      outlier_heads=(1,), seed=16),
+    configs.SMALL.with_(name="small_d64", D=64, seed=17),
 ]
 
 
@@ -185,3 +186,11 @@ def test_full_size_dense_sweep_large_key_offset():
     st = _full_size_check(w, "auto", per_frame_random=3)
     elig = st["eligible"].cpu().numpy().reshape(-1)
     assert elig[:18].all() and not elig[18:].any()
+
+
+def test_batch_of_two_at_720p_geometry():
+    """B = 2 with the 720p-like frame geometry (13 x 3600 tokens, window +-2,
+    reference frame 0), 2 heads each, one of them an outlier: the batch index
+    of every unit, stride and output row at full sequence length."""
+    w = configs.SR720.with_(name="sr720p_b2h2", B=2, H=2, outlier_heads=(1,), seed=18)
+    _full_size_check(w, "auto", per_frame_random=6)
