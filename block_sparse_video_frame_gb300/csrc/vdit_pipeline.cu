@@ -71,7 +71,7 @@ struct vdit_pipeline {
     int *first = nullptr;    // first head of each group, groups + 1 entries
     void *mem = nullptr;
     Slot slot[kSlots];
-    cudaStream_t s_in = nullptr, s_out = nullptr, s_cmp[kSlots] = {nullptr, nullptr};
+    cudaStream_t s_in = nullptr, s_out = nullptr, s_cmp[kSlots] = {};
     cudaEvent_t start = nullptr;
 };
 
@@ -256,11 +256,12 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
             }
         }
     }
-    if ((e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&p->s_cmp[0], cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&p->s_cmp[1], cudaStreamNonBlocking)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking)) != cudaSuccess) {
+    if ((e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming)) == cudaSuccess &&
+        (e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking)) == cudaSuccess)
+        e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking);
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i)
+        e = cudaStreamCreateWithFlags(&p->s_cmp[i], cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
         release(p);
         return cuda_fail(e, "vdit_pipeline_create: stream/event creation");
     }
