@@ -5,8 +5,8 @@ inputs are drawn). Nothing here computes any part of the attention method.
 
 Shapes follow the super-resolution and base-DiT attention described in
 "HeyGen x Google Cloud: Bringing Avatar IV to TPUs" ("Deleting the Mask":
-each frame's queries see a window of nearby frames plus one global reference
-frame; 720p/1080p output from "The Workload, and the Port"). The token counts
+a query attends to the frames within W of its own frame and to one fixed
+reference frame; 720p/1080p output from "The Workload, and the Port"). The token counts
 per frame are latent patch grids (20x20, 45x80, 68x120, 30x52).
 """
 from __future__ import annotations

@@ -13,12 +13,15 @@
 //     P.V product runs on the matrix unit.
 //
 // GB300 design. Persistent grid (one CTA per SM, 320 threads):
-//   warps 0-3, 4-7  softmax warpgroups, one per 128-row query tile; thread t
-//                   of a warpgroup owns TMEM lane t = query row t
-//   warp 8          TMA producer: Q tiles, then a 2-stage ring of K and V
-//                   tiles (128 keys x D, bf16, 128-byte swizzle)
-//   warp 9          TMEM allocator and single-thread tcgen05.mma issuer
-// A work unit is (b, h, segment, pair of query tiles). Both tiles of a unit
+//   warp 0          TMEM allocator and tcgen05.mma issuer (the warp walks the
+//                   schedule, one elected lane issues)
+//   warp 1          TMA producer: Q tiles, then a 2-stage ring of K tiles and a
+//                   3-stage ring of V tiles (128 keys x D, bf16, 128-byte swizzle)
+//   warps 2-5, 6-9  softmax warpgroups, one per 128-row query tile; thread t
+//                   of a warpgroup owns TMEM lane t = query row t (warp w reads
+//                   the lane quarter w % 4)
+// A work unit is (b, h, segment, pair of query tiles); the CTAs walk them two
+// heads at a time (see decode). Both tiles of a unit
 // lie in one segment (frames with identical key runs), share every K/V tile
 // and ping-pong on the tensor core:
 //   S0 = Q0 K_0^T, S1 = Q1 K_0^T, then for each key tile j:

@@ -6,8 +6,8 @@
 // its own transfer -> attention -> transfer chain, lets every middle transfer
 // hide behind another group's attention, leaving only the first transfer in
 // and the last transfer out exposed. Splitting by heads leaves the token order
-// (and so the frame-window mask) untouched: every group sees exactly the mask
-// it would have seen unsplit.
+// (and so the frame-window mask) untouched: each group gets the same mask as one launch
+// over all heads.
 //
 // On one GB300 the wire is the host link: Q, K, V of head group g are copied
 // in on one stream, the group's key statistics and attention run on the

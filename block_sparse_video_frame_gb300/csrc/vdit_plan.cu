@@ -4,8 +4,8 @@
 // (Fig. 3): a query in frame f sees the keys of frames g with |f - g| <= W
 // (clipped to the sequence) plus the reference frame. With a block size that
 // is a multiple of 16 and divides the frame's token span, each block is either
-// entirely live or entirely dead, and the reference frame's blocks are simply
-// more live blocks of the same pass.
+// entirely live or entirely dead, and the reference frame contributes
+// ordinary live blocks to the same pass.
 //
 // Two kernels build the plan on the device:
 //   plan_meta_kernel  per-frame key runs (at most two maximal runs of live key

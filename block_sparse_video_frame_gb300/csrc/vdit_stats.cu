@@ -1,13 +1,14 @@
 // Per-head key statistics and static-max eligibility.
 //
 // "HeyGen x Google Cloud: Bringing Avatar IV to TPUs", "Unchaining the
-// Softmax": a tiny array of precomputed norms lets every query row derive an
-// upper bound on its logits as it starts; centring the keys on their mean
-// tightens that bound without changing the softmax; heads whose bound is too
-// loose fall back to online softmax. This file computes, per (b, h):
+// Softmax": a few numbers per head, computed before attention, give every query
+// row an upper bound on its logits before its first key tile. Centring the keys
+// on their mean tightens the bound and leaves the softmax unchanged; a head with a
+// loose bound runs online softmax instead. This file computes, per (b, h):
 //   c    = (1/N) sum_j k_j          R  = max_j |k_j - c|
 //   Qm   = max_i |q_i|              G  = 2 * scale * Qm * R,  eligible = G <= tau
-// HBM-bound: K is read twice (the second read mostly from L2), Q once.
+// HBM-bound: K is read twice (the second read comes from L2 only while K fits
+// there; at 720p it does not), Q once.
 // Four launches, every reduction in a fixed order (bitwise reproducible):
 //   stats_pass1    per chunk of 512 rows: column sums of K, max |q|^2
 //   stats_mean     c = (sum of the chunk column sums) / N, per head

@@ -2,7 +2,7 @@
  * vdit.h -- C ABI of libvdit: frame-window + reference-frame block-sparse
  * self-attention for video diffusion transformers, hand-written for sm_103a.
  *
- * The operation is the super-resolution stage's sparse attention described in
+ * The operation is the sparse attention of the super-resolution stage described in
  * "HeyGen x Google Cloud: Bringing Avatar IV to TPUs":
  *   - "Deleting the Mask" (Fig. 3): every query in frame f attends to the keys
  *     of frames g with |f - g| <= W, plus one global reference frame. Blocks
@@ -12,7 +12,7 @@
  *   - "Unchaining the Softmax" (Fig. 4): the running max of online softmax is
  *     replaced by a precomputed per-row upper bound on the logits,
  *     scale * (q . c + |q| * max_j |k_j - c|), with c the per-head key mean;
- *     heads whose bound is too loose fall back to online softmax in the same
+ *     a head with a loose bound runs online softmax instead, in the same
  *     kernel.
  *   - "Proving the Pixels Didn't Change": the final P.V product runs in bf16.
  *
@@ -186,8 +186,8 @@ VDIT_API size_t vdit_key_stats_framed_workspace_size(const vdit_plan *plan, int3
                                                      int32_t D);
 
 /* Key statistics with the bound tightened per query segment ("Unchaining the
- * Softmax": the bound's guarantee holds for windowed sparse masks, where each
- * query row sees a different slice of the keys). For every segment s of the
+ * Softmax": the bound stays valid under windowed masks, where rows of different
+ * frames attend to different subsets of the keys). For every segment s of the
  * plan (frames sharing one key-run list; one frame for sparse windows, the
  * whole sequence when dense):
  *   k_mean[b,h,:]       = c, the mean of all N keys of the head    fp32 [B, H, D]

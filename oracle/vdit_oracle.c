@@ -7,8 +7,8 @@
  * shares no code, header, table or helper with the CUDA sources.
  *
  * Source: "HeyGen x Google Cloud: Bringing Avatar IV to TPUs"
- *   - "Deleting the Mask" (+ Fig. 3): each frame's queries see a window of
- *     nearby frames plus one global reference frame; blocks whose size divides
+ *   - "Deleting the Mask" (+ Fig. 3): a query attends to the frames within W of
+ *     its own frame and to one fixed reference frame; blocks whose size divides
  *     the frame's token span are entirely live or entirely dead.
  *   - "Unchaining the Softmax" (+ Fig. 4): mean-centred keys, the
  *     Cauchy-Schwarz row bound |q|*max|k - mean|, per-head eligibility.
@@ -316,9 +316,9 @@ void vo_attention_rows(const void *q, const void *k, const void *v, int dtype, i
     }
 }
 
-/* Per-query-frame key statistics ("Unchaining the Softmax": the bound's
- * guarantee holds for windowed sparse masks, where each query row sees a
- * different slice of the keys). For query frame f of head (b, h), with c the
+/* Per-query-frame key statistics ("Unchaining the Softmax": the bound stays
+ * valid under windowed masks, where rows of different frames attend to
+ * different subsets of the keys). For query frame f of head (b, h), with c the
  * key mean over all N keys of the head and J(f) = { j : mask(f*T, j) } the
  * keys that frame's queries see (tested token by token through vo_mask):
  *   R_f    = max_{j in J(f)} |k_j - c|_2

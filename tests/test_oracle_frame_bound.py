@@ -1,6 +1,6 @@
-"""Pins for the per-query-frame bound ("Unchaining the Softmax": the bound's
-guarantee extended to windowed sparse masks, where each row sees a different
-slice of the keys). Checked against numpy on an independent frame construction,
+"""Pins for the per-query-frame bound ("Unchaining the Softmax": the bound stays
+valid under windowed masks, where rows of different frames attend to different
+subsets of the keys). Checked against numpy on an independent frame construction,
 against the per-head statistics, and by the bound >= true max invariant."""
 import numpy as np
 import pytest

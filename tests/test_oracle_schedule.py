@@ -94,8 +94,8 @@ def test_schedule_csr_and_runs(F, T, W, ref):
 
 
 def test_misaligned_blocks_are_partial():
-    """'a frame's token span isn't a multiple of 128 ... live blocks straddle frame
-    boundaries': 128-token blocks over 400-token frames leave partial blocks, a
+    """Blocks of 128 tokens over frames whose token count 128 does not divide mix
+    live and dead token pairs ("Deleting the Mask"): 128-token blocks over 400-token frames leave partial blocks, a
     divisor of the span leaves none."""
     F, T, W, ref = 9, 400, 1, 0
     full, partial, dead = oracle.block_census(F, T, W, ref, 128)
