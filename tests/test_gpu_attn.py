@@ -90,7 +90,9 @@ def test_bf16_output_is_rounded_fp32_output():
 
 
 def test_deterministic_bytes():
-    """Two identical calls write identical bytes (the pages' 'dual baseline')."""
+    """Two identical calls write identical bytes. The pages' first quality gate
+    compares output hashes byte for byte for changes that keep the reduction
+    order ("Proving the Pixels Didn't Change")."""
     w = configs.SMALL
     q, k, v = synth.make_qkv(w)
     o1, l1, st, plan = run_gpu(w, q, k, v, out_dtype=torch.bfloat16)
