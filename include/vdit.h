@@ -333,6 +333,9 @@ VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int3
  * means o_host (and lse_host) are complete. An expired wait inside attention
  * is reported by vdit_plan_status on the plan. Arguments (pointers, strides,
  * scale finite and > 0, tau >= 0, mode) are checked before anything is queued.
+ * Consecutive batches overlap when they run on two pipelines, each with its
+ * own plan, on two streams: one batch's first copy-in and last copy-out then
+ * run beside the other batch's kernels (+6% at the 720p-like shape).
  * An error from a later step returns at once; copies and kernels of earlier
  * groups may still be in flight, and the host buffers must stay valid until
  * `stream` (or the device) is synchronised. Errors: VDIT_ERR_INVALID,
