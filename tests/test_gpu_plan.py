@@ -86,3 +86,36 @@ def test_segment_at_the_tile_pair_field_limit():
         vd.attn_plan(1, T + 128, 0, 0, 4096)
     assert ei.value.status == vd.VDIT_ERR_UNSUPPORTED
     assert "tile pairs" in str(ei.value)
+
+
+def test_plan_at_the_frame_limit():
+    """The largest plan in frames (4096, the meta kernel's per-frame arrays), with
+    16-token frames, window +-2 and reference frame 0. Expected values come from
+    the window rule itself: per frame the clipped window [f-2, f+2] plus frame 0
+    when it lies outside; one segment and one 16-row tile per frame; units of one
+    cost class per key count."""
+    F, T, W, ref, bs = 4096, 16, 2, 0, 16
+    plan = vd.attn_plan(F, T, W, ref, bs)
+    frames = []
+    for f in range(F):
+        lo, hi = max(0, f - W), min(F - 1, f + W)
+        runs = [[lo * T, (hi + 1) * T]]
+        if not lo <= ref <= hi:
+            runs = ([[ref * T, (ref + 1) * T], [lo * T, (hi + 1) * T]] if lo > ref + 1
+                    else [[ref * T, (hi + 1) * T]])
+        frames.append(runs[0] + (runs[1] if len(runs) > 1 else [0, 0]))
+    want_runs = np.array(frames, dtype=np.int32)
+    assert np.array_equal(plan.frame_runs().cpu().numpy(), want_runs)
+    keys = [(r[1] - r[0]) + (r[3] - r[2]) for r in frames]
+    assert plan.info.live_pairs == sum(keys) * T
+    assert plan.info.nnz == sum(keys) // bs
+    segs = plan.segments().cpu().numpy()
+    units = plan.units().cpu().numpy().astype(np.int64)
+    assert plan.info.n_segments == F and len(units) == F
+    assert sorted(int(s[0]) for s in segs) == [f * T for f in range(F)]
+    # longest first: the unit key counts never increase, and each class has one count
+    ukeys = np.array([segs[u >> 16][7] for u in units])
+    assert (np.diff(ukeys) <= 0).all()
+    assert sorted(ukeys.tolist(), reverse=True) == sorted(keys, reverse=True)
+    cls = plan.class_offsets().cpu().numpy()
+    assert len(cls) - 1 == len(set(keys))
