@@ -771,7 +771,10 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 // Both head dims request the D = 128 shared-memory size: one CTA (and so one
 // TMEM owner) per SM.
-constexpr int kSmemRequest = Layout<128>::kAlloc;
+constexpr int kSmemRequest = Layout<128>::kAlloc;   // both head dims launch with this size
+static_assert(Layout<64>::kBytes <= Layout<64>::kAlloc && Layout<64>::kAlloc <= kSmemRequest,
+              "the D = 64 layout must fit the shared-memory request");
+static_assert(kSmemRequest <= 227 * 1024, "shared memory beyond the per-CTA limit");
 
 template <int D>
 cudaError_t prepare_kernel(int device) {
