@@ -72,10 +72,10 @@ def test_framed_attention_parity(w):
                 lse.reshape(-1).double().cpu().numpy(), lse_ref, w.name)
 
 
-def test_framed_full_size_720p_sampled():
-    w = configs.SR720
+@pytest.mark.parametrize("w", [configs.SR720, configs.SR1080], ids=lambda w: w.name)
+def test_framed_full_size_sampled(w):
     q, k, v = synth.make_qkv(w)
-    rows = stratified_rows(w)
+    rows = stratified_rows(w, per_frame_random=13 if w is configs.SR720 else 6)
     o_ref, lse_ref, _ = oracle_rows(w, q, k, v, rows)
     plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
     qd, kd, vd_ = q.cuda(), k.cuda(), v.cuda()
@@ -83,7 +83,7 @@ def test_framed_full_size_720p_sampled():
     o, lse = vd.attn_fwd(plan, qd, kd, vd_, st, w.scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert plan.status() == 0
-    check_close(gather_rows(o, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref, "sr720p framed")
+    check_close(gather_rows(o, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref, f"{w.name} framed")
     # at least as many eligible (head, segment) pairs as per-head eligibility gives
     head = vd.key_stats(qd, kd, w.scale, TAU)["eligible"].cpu().numpy()
     seg = st["seg_eligible"].cpu().numpy()
