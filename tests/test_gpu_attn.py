@@ -15,6 +15,8 @@ import torch
 import block_sparse_video_frame_gb300 as vd
 from block_sparse_video_frame_gb300 import configs, synth
 
+import oracle
+
 from parity_util import check_close, gather_rows, oracle_rows, stratified_rows
 
 pytestmark = pytest.mark.gpu
@@ -196,3 +198,55 @@ def test_batch_of_two_at_720p_geometry():
     of every unit, stride and output row at full sequence length."""
     w = configs.SR720.with_(name="sr720p_b2h2", B=2, H=2, outlier_heads=(1,), seed=18)
     _full_size_check(w, "auto", per_frame_random=6)
+
+
+def _worst_case_gap_inputs(s_heads, R=16.0, T=128, F=4, D=128, seed=31):
+    """Block-diagonal mask (W = 0, no reference frame). In every head the keys of
+    frame 0 sit at c - R e0 and the keys of frames 1..3 at c + (R/3) e0, so the
+    key mean is c and the largest centred key norm is R. Every query of the head
+    is s e0. A query in frame 0 sees only the keys of frame 0, so its true max
+    logit is scale (q.c - s R) while its bound is scale (q.c + s R): the gap is
+    2 scale s R = G, the worst case the eligibility rule allows for."""
+    g = torch.Generator().manual_seed(seed)
+    H = len(s_heads)
+    c = torch.zeros(D, dtype=torch.float64)
+    c[1:4] = torch.tensor([0.5, -0.25, 0.125], dtype=torch.float64)
+    q = torch.zeros((1, H, F * T, D), dtype=torch.float64)
+    k = c.expand(1, H, F * T, D).clone()
+    for h, s in enumerate(s_heads):
+        q[0, h, :, 0] = s
+        k[0, h, :T, 0] -= R
+        k[0, h, T:, 0] += R / 3
+    v = torch.randn((1, H, F * T, D), generator=g, dtype=torch.float64)
+    w = configs.Workload("worst_gap", B=1, H=H, D=D, F=F, T=T, W=0, ref=-1, block_size=16,
+                         outlier_heads=(), seed=seed)
+    return w, (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+
+
+def test_static_path_at_the_worst_case_gap():
+    """'Unchaining the Softmax' eligibility: with G = 2 scale Qmax R <= 64 no row's
+    exponentials can underflow, even when a row's true max sits the full G below
+    its bound. Head 0 is built at G = 60 with that worst-case gap on every row of
+    frame 0 (the static path must match the oracle); head 1 at G = 150 is
+    ineligible and must take the online path."""
+    w, (q, k, v) = _worst_case_gap_inputs([21.25, 53.0])
+    ost = oracle.key_stats(q, k, w.scale, 64.0)
+    G = ost["G"].reshape(-1)
+    assert 59.0 < G[0] < 61.0 and G[1] > 140.0
+    o_ref, lse_ref, mx = oracle_rows(w, q, k, v)
+    m = oracle.row_bounds(q, ost["c"], ost["R"], w.scale).reshape(-1)
+    gap0 = (m - mx)[: w.T]                                  # head 0, frame 0 rows
+    assert np.allclose(gap0, G[0], rtol=1e-6), "the construction must reach the worst case"
+    for mode in ("auto", "static", "online"):
+        if mode == "static":
+            # forcing the bound is only claimed for eligible heads: check head 0 only
+            o, lse, st, _ = run_gpu(w.with_(H=1), q[:, :1].contiguous(), k[:, :1].contiguous(),
+                                    v[:, :1].contiguous(), mode=mode)
+            n = w.N
+            check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref[:n],
+                        lse.reshape(-1).double().cpu().numpy(), lse_ref[:n], f"worst gap {mode}")
+            continue
+        o, lse, st, _ = run_gpu(w, q, k, v, mode=mode)
+        check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref,
+                    lse.reshape(-1).double().cpu().numpy(), lse_ref, f"worst gap {mode}")
+        assert st["eligible"].cpu().numpy().reshape(-1).tolist() == [1, 0]
