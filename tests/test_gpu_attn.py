@@ -250,3 +250,28 @@ def test_static_path_at_the_worst_case_gap():
         check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref,
                     lse.reshape(-1).double().cpu().numpy(), lse_ref, f"worst gap {mode}")
         assert st["eligible"].cpu().numpy().reshape(-1).tolist() == [1, 0]
+
+
+@pytest.mark.parametrize("zero", ["k", "q"])
+def test_degenerate_zero_keys_or_queries(zero):
+    """All keys zero (c = 0, R = 0, G = 0: eligible, and the bound equals the true
+    max 0) or all queries zero (every logit 0): every p is 1, so O is the plain
+    mean of V over the row's live keys and LSE = ln |J(i)|. Expected values from
+    the frame-window rule directly."""
+    w = configs.Workload("zero_" + zero, B=1, H=2, D=128, F=6, T=48, W=1, ref=0, block_size=16,
+                         outlier_heads=(), seed=41)
+    q, k, v = synth.make_qkv(w)
+    if zero == "k":
+        k = torch.zeros_like(k)
+    else:
+        q = torch.zeros_like(q)
+    o, lse, st, _ = run_gpu(w, q, k, v)
+    assert st["eligible"].cpu().numpy().all()
+    vv = v.double().numpy()[0]                          # [H, N, D]
+    f = np.arange(w.N) // w.T
+    live = (np.abs(f[:, None] - f[None, :]) <= w.W) | (f[None, :] == w.ref)   # [N, N]
+    want = np.einsum("ij,hjd->hid", live.astype(np.float64), vv) / live.sum(1)[None, :, None]
+    got = o[0].double().cpu().numpy()
+    assert np.abs(got - want).max() < 1e-5, np.abs(got - want).max()
+    np.testing.assert_allclose(lse[0].double().cpu().numpy(),
+                               np.broadcast_to(np.log(live.sum(1)), (w.H, w.N)), atol=1e-5)
