@@ -275,3 +275,30 @@ def test_degenerate_zero_keys_or_queries(zero):
     assert np.abs(got - want).max() < 1e-5, np.abs(got - want).max()
     np.testing.assert_allclose(lse[0].double().cpu().numpy(),
                                np.broadcast_to(np.log(live.sum(1)), (w.H, w.N)), atol=1e-5)
+
+
+def test_online_rescale_under_a_rising_max():
+    """Online softmax with the row max rising on every key tile (FORCE_ONLINE, one
+    1536-token frame = 12 key tiles). Head 0: logits climb ~150 nats along the keys,
+    so each tile lifts the running max past the lazy-rescale threshold (2^8) and O
+    is rescaled every tile. Head 1: the climb is 60 nats, so some tiles stay under the
+    threshold and their p run above 1 against a stale max. Head 2: the logits fall,
+    so the first tile holds the max. All rows against the oracle."""
+    T, D = 1536, 128
+    w = configs.Workload("rising_max", B=1, H=3, D=D, F=1, T=T, W=0, ref=0, block_size=16,
+                         outlier_heads=(), seed=43)
+    g = torch.Generator().manual_seed(43)
+    s = 8.0                                          # |q| along e0
+    ramp = torch.arange(T, dtype=torch.float64) / T
+    q = torch.zeros((1, 3, T, D), dtype=torch.float64)
+    q[..., 0] = s
+    q[..., 1:] = 0.05 * torch.randn((1, 3, T, D - 1), generator=g, dtype=torch.float64)
+    k = 0.05 * torch.randn((1, 3, T, D), generator=g, dtype=torch.float64)
+    for h, total_nats in enumerate((150.0, 60.0, -150.0)):
+        k[0, h, :, 0] += total_nats / (w.scale * s) * ramp
+    v = torch.randn((1, 3, T, D), generator=g, dtype=torch.float64)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v)
+    o, lse, _, _ = run_gpu(w, q, k, v, mode="online")
+    check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref,
+                lse.reshape(-1).double().cpu().numpy(), lse_ref, "rising max")
