@@ -425,7 +425,8 @@ def qkv_status(workspace, stream=None) -> int:
 class Pipeline:
     """Head-group pipelined attention over HOST tensors ("Hiding the Collective",
     Fig. 2): each group of heads is copied in, gets its key statistics and
-    attention, and is copied out, on three streams, so the middle transfers
+    attention, and is copied out, on four streams (copy-in, two compute, copy-out),
+    so the middle transfers
     hide behind other groups' attention (vdit_pipeline_*)."""
 
     def __init__(self, plan: "Plan", B, H, D, groups):
