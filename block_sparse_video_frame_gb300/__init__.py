@@ -426,8 +426,7 @@ class Pipeline:
     """Head-group pipelined attention over HOST tensors ("Hiding the Collective",
     Fig. 2): each group of heads is copied in, gets its key statistics and
     attention, and is copied out, on four streams (copy-in, two compute, copy-out),
-    so the middle transfers
-    hide behind other groups' attention (vdit_pipeline_*)."""
+    so the middle transfers hide behind other groups' attention (vdit_pipeline_*)."""
 
     def __init__(self, plan: "Plan", B, H, D, groups):
         """groups: a count (equal split), 0 (the library's tapered schedule) or a
