@@ -62,7 +62,9 @@ ALL = (TINY, SMALL, SR720, SR1080, DENSE)
 # 720p-like geometry with 8 heads (Q+K+V = 288 MB, still larger than L2): the
 # case profiled with the full ncu section set.
 SR720_H8 = SR720.with_(name="sr720p_h8", H=8, outlier_heads=(7,))
-BY_NAME = {w.name: w for w in ALL + (SR720_H8,)}
+# the same hidden size split into 48 heads of 64 (the D = 64 kernel at scale)
+SR720_D64 = SR720.with_(name="sr720p_d64", D=64, H=48, outlier_heads=(47,))
+BY_NAME = {w.name: w for w in ALL + (SR720_H8, SR720_D64)}
 
 
 def dense_sweep():

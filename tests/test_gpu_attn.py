@@ -133,7 +133,8 @@ def test_lse_optional():
     check_close(o.reshape(-1, w.D).double().cpu().numpy(), o_ref, what="no-lse")
 
 
-@pytest.mark.parametrize("w", [configs.SR720, configs.SR1080, configs.DENSE], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [configs.SR720, configs.SR1080, configs.DENSE, configs.SR720_D64],
+                         ids=lambda w: w.name)
 def test_full_size_sampled_rows(w):
     """Full-size workloads in the benchmark's launch configuration (AUTO mode,
     bf16 output as timed, fp32 output for the gate), on stratified row samples."""
