@@ -94,12 +94,19 @@ def load_peaks():
 
 
 def attn_kernel_source_hash():
-    """sha256 (first 16 hex digits) of the attention kernel's sources."""
+    """sha256 (first 16 hex digits) of the attention kernel's sources with the
+    line comments, trailing blanks and empty lines removed: a comment edit leaves
+    the compiled kernel, and so the recorded counters, unchanged. (The sources
+    use only // comments and hold no // inside a string literal.)"""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("vdit_attn.cu", "vdit_ptx.cuh"):
-        with open(os.path.join(ROOT, "block_sparse_video_frame_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "block_sparse_video_frame_gb300", "csrc", f), encoding="utf-8") as fh:
+            for line in fh:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

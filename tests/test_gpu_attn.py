@@ -3,9 +3,9 @@
 Full-row comparisons on cases the oracle finishes in seconds (several query and
 key tiles, ragged key tails, segments shorter than a tile, dense with a key
 count that is not a multiple of 16, no reference frame, reference frame in the
-middle, D = 64 and 128, batch > 1, strided inputs); stratified row samples at
-the full 720p-like, 1080p-like and dense sizes in the launch configuration the
-benchmark times. Tolerances: max-abs 1e-2, mean-abs 1e-3 on O (fp32 output),
+middle or last, 16-token frames, D = 64 and 128, batch > 1, strided inputs);
+stratified row samples at the full 720p-like, 1080p-like and dense sizes in the
+launch configuration the benchmark times. Tolerances: max-abs 1e-2, mean-abs 1e-3 on O (fp32 output),
 1e-3 on LSE; the bf16 output equals the fp32 output rounded to nearest even.
 """
 import numpy as np
@@ -39,6 +39,10 @@ SMALL_CASES = [
     configs.Workload("wide_w", B=1, H=2, D=64, F=10, T=64, W=3, ref=0, block_size=64,
                      outlier_heads=(1,), seed=16),
     configs.SMALL.with_(name="small_d64", D=64, seed=17),
+    configs.Workload("ref_last", B=1, H=2, D=128, F=8, T=48, W=1, ref=7, block_size=16,
+                     outlier_heads=(1,), seed=18),
+    configs.Workload("short_frames_ref_mid", B=1, H=3, D=64, F=7, T=16, W=2, ref=3, block_size=16,
+                     outlier_heads=(2,), seed=19),
 ]
 
 
