@@ -64,7 +64,9 @@ ALL = (TINY, SMALL, SR720, SR1080, DENSE)
 SR720_H8 = SR720.with_(name="sr720p_h8", H=8, outlier_heads=(7,))
 # the same hidden size split into 48 heads of 64 (the D = 64 kernel at scale)
 SR720_D64 = SR720.with_(name="sr720p_d64", D=64, H=48, outlier_heads=(47,))
-BY_NAME = {w.name: w for w in ALL + (SR720_H8, SR720_D64)}
+# 16 heads of 64: the bytes and FLOPs of sr720p_h8 at the other head dim (profiling size)
+SR720_D64_H16 = SR720.with_(name="sr720p_d64_h16", D=64, H=16, outlier_heads=(15,))
+BY_NAME = {w.name: w for w in ALL + (SR720_H8, SR720_D64, SR720_D64_H16)}
 
 
 def dense_sweep():
