@@ -848,7 +848,7 @@ def main(argv=None):
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "traffic": (args.traffic_bytes if args.traffic_bytes is not None
                                      else recorded_traffic(w.name)),
-                         "kernel": "attn_fwd_kernel<128>", "peak_source":
+                         "kernel": f"attn_fwd_kernel<{w.D}>", "peak_source":
                          f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
             "gpu_launches": LAUNCHES_PER_STEP * args.steps,
             "clocks": clocks,
