@@ -369,7 +369,7 @@ def run_sweep(args):
     from block_sparse_video_frame_gb300 import configs, synth
     torch.cuda.set_device(0)
     vd.load_library()
-    workloads = [configs.SR720, configs.SR1080, configs.DENSE] + configs.dense_sweep()
+    workloads = [configs.SR720, configs.SR1080, configs.DENSE, configs.SR720_D64] + configs.dense_sweep()
     for w in workloads:
         q, k, v = (t.cuda() for t in synth.make_qkv(w))
         plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
