@@ -379,23 +379,33 @@ def run_sweep(args):
         lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=q.device)
         stf = vd.key_stats_framed(plan, q, k, w.scale)
         elig = st["eligible"].float().mean().item()
-        for mode in ("auto", "online", "static", "auto_framed"):
-            stats = stf if mode == "auto_framed" else st
-            md = "auto" if mode == "auto_framed" else mode
-            for _ in range(3):
-                vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = 10
-            e0.record()
-            for _ in range(n):
-                vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
-            e1.record()
-            torch.cuda.synchronize()
-            if plan.status() != 0:
-                raise RuntimeError(f"expired wait in {w.name} {mode}")
-            ms = e0.elapsed_time(e1) / n
+        modes = ("auto", "online", "static", "auto_framed")
+        # The modes are timed in rounds (each round times every mode once, in a
+        # rotated order) and each mode reports its median round, so the board's
+        # drift toward its power limit during the run does not favour one mode.
+        rounds = {m: [] for m in modes}
+        for rnd in range(3):
+            for i in range(len(modes)):
+                mode = modes[(i + rnd) % len(modes)]
+                stats = stf if mode == "auto_framed" else st
+                md = "auto" if mode == "auto_framed" else mode
+                for _ in range(3):
+                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                n = 10
+                e0.record()
+                for _ in range(n):
+                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
+                e1.record()
+                torch.cuda.synchronize()
+                if plan.status() != 0:
+                    raise RuntimeError(f"expired wait in {w.name} {mode}")
+                rounds[mode].append(e0.elapsed_time(e1) / n)
+        for mode in modes:
+            ms = statistics.median(rounds[mode])
             print(json.dumps({"workload": w.name, "mode": mode, "ms_per_call": ms,
+                              "ms_rounds": rounds[mode],
                               "tflops": flops / (ms * 1e-3) / 1e12,
                               "eligible_fraction": (stf["seg_eligible"].float().mean().item()
                                                     if mode == "auto_framed" else elig),
