@@ -3,10 +3,12 @@
 Full-row comparisons on cases the oracle finishes in seconds (several query and
 key tiles, ragged key tails, segments shorter than a tile, dense with a key
 count that is not a multiple of 16, no reference frame, reference frame in the
-middle or last, 16-token frames, D = 64 and 128, batch > 1, strided inputs);
-stratified row samples at the full 720p-like, 1080p-like and dense sizes in the
-launch configuration the benchmark times. Tolerances: max-abs 1e-2, mean-abs 1e-3 on O (fp32 output),
-1e-3 on LSE; the bf16 output equals the fp32 output rounded to nearest even.
+middle or last, 16-token frames, a single token, D = 64 and 128, batch > 1,
+strided inputs); stratified row samples at the full 720p-like, 1080p-like and
+dense sizes, and the 720p-like geometry at D = 64, in the launch configuration
+the benchmark times. Tolerances: max-abs 1e-2, mean-abs 1e-3 on O (fp32
+output), 1e-3 on LSE; the bf16 output equals the fp32 output rounded to nearest
+even.
 """
 import numpy as np
 import pytest
@@ -43,6 +45,11 @@ SMALL_CASES = [
                      outlier_heads=(1,), seed=18),
     configs.Workload("short_frames_ref_mid", B=1, H=3, D=64, F=7, T=16, W=2, ref=3, block_size=16,
                      outlier_heads=(2,), seed=19),
+    # one token (the output is that token's value row) and a 40-token dense sequence
+    configs.Workload("one_token", B=1, H=2, D=128, F=1, T=1, W=0, ref=0, block_size=16,
+                     outlier_heads=(), seed=20),
+    configs.Workload("dense_n40", B=1, H=2, D=64, F=5, T=8, W=4, ref=0, block_size=16,
+                     outlier_heads=(1,), seed=21),
 ]
 
 

@@ -19,6 +19,7 @@ CASES = [
     (21, 1560, 20, 0, 16), (21, 1560, 20, 0, 128), # dense base DiT (ragged last block)
     (7, 16, 2, 3, 16), (6, 32, 0, -1, 32), (1, 64, 0, 0, 16), (8, 48, 1, 7, 16),
     (5, 24, 4, 0, 16), (12, 32, 3, -1, 16),
+    (1, 1, 0, 0, 16), (5, 8, 4, 0, 16), (3, 5, 2, -1, 16),   # one token; tiny dense sequences
 ]
 
 
