@@ -549,6 +549,29 @@ def run_pipeline_sweep(args):
         return a.elapsed_time(b) / n
 
     n = max(3, min(args.steps, 10))
+
+    # the host link alone: pinned host <-> device copies of one 288 MB tensor (or
+    # three, on three streams), each copy on its own stream joined to the timing stream
+    def link_gbs(copies):
+        side = [torch.cuda.Stream() for _ in copies]
+
+        def once():
+            for sd in side:
+                sd.wait_stream(stream)
+            for sd, (dst, src) in zip(side, copies):
+                with torch.cuda.stream(sd):
+                    dst.copy_(src, non_blocking=True)
+            for sd in side:
+                stream.wait_stream(sd)
+        ms = timed(once, n)
+        return sum(src.numel() * src.element_size() for _, src in copies) / (ms * 1e-3) / 1e9
+
+    print(json.dumps({"workload": w.name, "host_link_gbs": {
+        "h2d_1_stream": link_gbs([(q, q_h)]),
+        "h2d_3_streams": link_gbs([(q, q_h), (k, k_h), (v, v_h)]),
+        "d2h_1_stream": link_gbs([(o_h, o)]),
+        "both_directions_total": link_gbs([(q, q_h), (o_h, o)])},
+        "bytes_per_tensor": q_h.numel() * q_h.element_size()}), flush=True)
     dev_ms = timed(lambda: (vd.key_stats(q, k, w.scale, out=st),
                             vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False)), n)
     moved = 4 * q_h.numel() * q_h.element_size()
