@@ -443,13 +443,18 @@ class Pipeline:
         self._h = h
         self.plan = plan            # the pipeline keeps using the plan's device schedule
         self.B, self.H, self.D, self.groups = int(B), int(H), int(D), groups
+        # host tensors of runs whose copies may still be in flight, each with an
+        # event recorded after the run: they stay referenced until it completes
+        self._inflight = []
 
     def run(self, q_h, k_h, v_h, o_h, scale, lse_h=None, tau=64.0, mode="auto", stream=None):
         """q_h, k_h, v_h, o_h: bf16 CPU tensors (pinned for overlap) indexed
         [B, H, N, D] with identical strides and d contiguous; lse_h: optional fp32
         [B, H, N] contiguous CPU tensor. Asynchronous: synchronise the stream
-        before reading o_h."""
+        before reading o_h. The host tensors stay referenced by the pipeline until
+        the run's copies have completed."""
         import torch
+        self._inflight = [(ev, held) for ev, held in self._inflight if not ev.query()]
         ts = (q_h, k_h, v_h, o_h)
         for name, t in zip("qkvo", ts):
             if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 4 or t.dtype != torch.bfloat16:
@@ -461,15 +466,21 @@ class Pipeline:
         if lse_h is not None and (lse_h.dtype != torch.float32 or not lse_h.is_contiguous()
                                   or tuple(lse_h.shape) != (self.B, self.H, self.plan.num_tokens)):
             raise ValueError("lse_h must be a contiguous fp32 [B, H, N] CPU tensor")
-        _check(load_library().vdit_pipeline_run(
+        status = load_library().vdit_pipeline_run(
             self._h, _ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h), _strides(q_h),
-            float(scale), float(tau), MODES[mode], _stream(stream)))
+            float(scale), float(tau), MODES[mode], _stream(stream))
+        # held even when the call failed part-way: copies queued before the error still run
+        ev = torch.cuda.Event(enable_timing=False)
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+        self._inflight.append((ev, (q_h, k_h, v_h, o_h, lse_h)))
+        _check(status)
         return o_h
 
     def close(self):
         if getattr(self, "_h", None) and self._h.value:
-            load_library().vdit_pipeline_destroy(self._h)
+            load_library().vdit_pipeline_destroy(self._h)   # waits for the pipeline's streams
             self._h = ctypes.c_void_p()
+        self._inflight = []
 
     def __del__(self):
         try:
