@@ -330,7 +330,8 @@ VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int3
  * use tau as in vdit_key_stats; mode as in vdit_attn_fwd. Asynchronous with
  * respect to the host: the work is ordered after everything already queued on
  * `stream`, and `stream` waits for all of it, so a synchronisation of `stream`
- * means o_host (and lse_host) are complete. An expired wait inside attention
+ * means o_host (and lse_host) are complete; every host buffer stays owned by
+ * the caller and must stay valid until then. An expired wait inside attention
  * is reported by vdit_plan_status on the plan. Arguments (pointers, strides,
  * scale finite and > 0, tau >= 0, mode) are checked before anything is queued.
  * Consecutive batches overlap when they run on two pipelines, each with its
