@@ -47,7 +47,9 @@ size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // the only transfers left exposed, so they are the smallest; each later copy-in
 // (about 0.6 of a head's attention time per head on the host link of a GB300)
 // still hides behind the previous, smaller group's kernels. Heads beyond the
-// ramps that do not fill a group of c join the middle groups one each.
+// ramps that do not fill a group of c are spread over the middle groups, one
+// more per group in turn (a group takes several when there are fewer middle
+// groups than leftover heads).
 // Returns the group count (sizes in out[]), or 0 when H is too small for the
 // ramps (the caller then splits evenly into groups of about c).
 constexpr int kTaperCap = 4;
@@ -56,9 +58,11 @@ int tapered_split(int H, int *out) {
     if (H < 2 * ramp + kTaperCap) return 0;
     const int mid = H - 2 * ramp, nmid = mid / kTaperCap, extra = mid % kTaperCap;
     if (2 * (kTaperCap - 1) + nmid > 64) return 0;
+    // nmid >= 1 here, since mid >= c
+    const int each = kTaperCap + extra / nmid, rest = extra % nmid;
     int g = 0;
     for (int i = 1; i < kTaperCap; ++i) out[g++] = i;
-    for (int i = 0; i < nmid; ++i) out[g++] = kTaperCap + (i < extra ? 1 : 0);
+    for (int i = 0; i < nmid; ++i) out[g++] = each + (i < rest ? 1 : 0);
     for (int i = kTaperCap - 1; i >= 1; --i) out[g++] = i;
     return g;
 }
@@ -220,6 +224,12 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
         p->hg = (H + groups - 1) / groups;
         p->groups = (H + p->hg - 1) / p->hg;
         for (int g = 0; g <= p->groups; ++g) p->first[g] = g * p->hg < H ? g * p->hg : H;
+    }
+    if (p->first[p->groups] != H) {   // every schedule above covers the H heads exactly
+        const int covered = p->first[p->groups];
+        release(p);
+        set_error("vdit_pipeline_create: head groups cover %d of %d heads", covered, H);
+        return VDIT_ERR_INVALID;
     }
     const size_t N = (size_t)p->N, hg = (size_t)p->hg;
     const size_t t_bytes = align_up((size_t)B * hg * N * D * 2);

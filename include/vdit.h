@@ -310,8 +310,8 @@ typedef struct vdit_pipeline vdit_pipeline;
  * into `groups` head groups: group_heads[g] heads each (host array of `groups`
  * positive counts summing to H), or, when group_heads is NULL, ceil(H / groups)
  * heads each (the last may be smaller). groups = 0 with group_heads NULL picks
- * a tapered schedule: 1, 2, 3 heads, then groups of 4 (one more head in the
- * first ones when 4 does not divide the rest), then 3, 2, 1 heads, so that the
+ * a tapered schedule: 1, 2, 3 heads, then groups of 4 (the heads left over
+ * spread one at a time over those groups), then 3, 2, 1 heads, so that the
  * exposed first copy-in and last copy-out are one head each; for H < 16 an
  * even split into groups of about 4. Allocates two device slots (Q, K, V, O,
  * LSE, statistics and their workspace for the largest group each), four streams

@@ -45,6 +45,27 @@ def test_pipeline_equals_single_launch(groups):
     pipe.close()
 
 
+@pytest.mark.parametrize("H", [16, 17, 18, 19, 23])
+def test_tapered_default_covers_every_head(H):
+    """The default schedule (1, 2, 3 heads, groups of 4 with the leftover heads
+    spread over them, 3, 2, 1) for head counts whose leftovers outnumber the
+    middle groups: every head's output equals the single launch bit for bit."""
+    w = configs.Workload(f"taper_h{H}", B=1, H=H, D=64, F=3, T=64, W=1, ref=0, block_size=64,
+                         outlier_heads=(H - 1,), seed=40 + H)
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    o_ref, _ = device_reference(w, q, k, v, plan)
+    q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+    o_h = pinned_like(q)
+    o_h.fill_(float("nan"))
+    pipe = vd.Pipeline(plan, w.B, w.H, w.D, 0)
+    pipe.run(q_h, k_h, v_h, o_h, w.scale)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
+    pipe.close()
+
+
 def test_pipeline_token_major_host_layout():
     """Host tensors stored [B, N, H, D] (the sequence-sharded layout a projection
     emits) and passed as [B, H, N, D] views: same bytes as the device path."""
