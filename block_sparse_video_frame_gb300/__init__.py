@@ -32,7 +32,7 @@ EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_p
             "vdit_key_stats_framed", "vdit_attn_fwd_framed", "vdit_qkv_fold_gamma",
             "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status",
             "vdit_pipeline_create", "vdit_pipeline_run", "vdit_pipeline_destroy",
-            "vdit_set_alloc_fail_after")
+            "vdit_pipeline_default_groups", "vdit_set_alloc_fail_after")
 
 
 class VditError(RuntimeError):
@@ -115,6 +115,8 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_pipeline_run.restype = ctypes.c_int
         lib.vdit_pipeline_destroy.argtypes = [vp]
         lib.vdit_pipeline_destroy.restype = None
+        lib.vdit_pipeline_default_groups.argtypes = [i32, vp, i32]
+        lib.vdit_pipeline_default_groups.restype = i32
         lib.vdit_set_alloc_fail_after.argtypes = [i32]
         lib.vdit_set_alloc_fail_after.restype = None
         _lib = lib
@@ -487,6 +489,16 @@ class Pipeline:
             self.close()
         except Exception:
             pass
+
+
+def default_groups(H: int) -> list:
+    """Head counts of the groups that Pipeline(..., groups=0) uses for H heads
+    (vdit_pipeline_default_groups; host only)."""
+    out = (ctypes.c_int32 * max(1, int(H)))()
+    n = load_library().vdit_pipeline_default_groups(int(H), ctypes.cast(out, ctypes.c_void_p), len(out))
+    if n <= 0:
+        raise ValueError(f"no default schedule for H={H}")
+    return [int(out[i]) for i in range(n)]
 
 
 def set_alloc_fail_after(n: int) -> None:

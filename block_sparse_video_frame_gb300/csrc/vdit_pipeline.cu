@@ -69,6 +69,25 @@ int tapered_split(int H, int *out) {
 
 }  // namespace
 
+// The schedule vdit_pipeline_create picks for groups = 0: the tapered split when
+// H allows the ramps, else ceil(H / c) groups of equal size (the last may be
+// smaller), by the same rules as the create call below.
+extern "C" int32_t vdit_pipeline_default_groups(int32_t H, int32_t *out, int32_t cap) {
+    if (H < 1 || !out || cap < 1) return 0;
+    int taper[64];
+    int n = tapered_split(H, taper);
+    if (n > 0) {
+        if (n > cap) return 0;
+        for (int i = 0; i < n; ++i) out[i] = taper[i];
+        return n;
+    }
+    const int groups = (H + kTaperCap - 1) / kTaperCap, hg = (H + groups - 1) / groups;
+    n = (H + hg - 1) / hg;
+    if (n > cap) return 0;
+    for (int i = 0; i < n; ++i) out[i] = (i + 1) * hg <= H ? hg : H - i * hg;
+    return n;
+}
+
 struct vdit_pipeline {
     const vdit_plan *plan = nullptr;
     int B = 0, H = 0, D = 0, N = 0, groups = 0, hg = 0, device = -1;

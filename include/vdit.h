@@ -319,6 +319,13 @@ typedef struct vdit_pipeline vdit_pipeline;
  * VDIT_ERR_INVALID (null plan or out, B or H < 1, groups outside [0, H], bad
  * group_heads, plan from another device), VDIT_ERR_UNSUPPORTED (D),
  * VDIT_ERR_NOMEM, VDIT_ERR_CUDA. */
+/* The head-group schedule that vdit_pipeline_create picks for H heads when
+ * groups = 0 and group_heads is NULL: writes the head count of each group to
+ * out[0 .. n-1] (host array of cap entries) and returns n, or returns 0 and
+ * writes nothing when H < 1, out is NULL or cap < n. Host only: no device
+ * work, no allocation, callable without a GPU. */
+VDIT_API int32_t vdit_pipeline_default_groups(int32_t H, int32_t *out, int32_t cap);
+
 VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int32_t H, int32_t D,
                                           int32_t groups, const int32_t *group_heads,
                                           vdit_pipeline **out);

@@ -146,3 +146,25 @@ def test_prologue_entry_points_reject_bad_arguments(lib):
         st = lib.vdit_qkv_prologue(p, s2, p, p, p, p, p, s3, s3, s3, 1, 16, 1024, 8, 128, eps, p, 1 << 20, None)
         assert st == vd.VDIT_ERR_INVALID and "eps" in lib.vdit_last_error().decode()
     assert lib.vdit_qkv_fold_gamma(None, p, p, 4, 8, None) == vd.VDIT_ERR_INVALID
+
+
+def test_default_head_groups_cover_every_head(lib):
+    """The pipeline's default schedule (host only): the groups cover the H heads
+    exactly; from H = 16 (while the groups stay within 64) it ramps 1, 2, 3 up
+    and 3, 2, 1 down around middle groups of at least 4 that differ by at most
+    one head; otherwise it is an even split into groups of about 4."""
+    for H in range(1, 400):
+        g = vd.default_groups(H)
+        assert sum(g) == H and min(g) >= 1, (H, g)
+        mid = g[3:-3]
+        if H >= 16 and 6 + (H - 12) // 4 <= 64:   # the ramps fit the 64-group limit
+            assert g[:3] == [1, 2, 3] and g[-3:] == [3, 2, 1], (H, g)
+            assert min(mid) >= 4 and max(mid) - min(mid) <= 1, (H, g)
+        else:
+            assert max(g) <= -(-H // -(-H // 4)) and len(g) == -(-H // max(g)), (H, g)
+    assert vd.default_groups(24) == [1, 2, 3, 4, 4, 4, 3, 2, 1]
+    assert vd.default_groups(19) == [1, 2, 3, 7, 3, 2, 1]
+    assert vd.default_groups(8) == [4, 4]
+    buf = (ctypes.c_int32 * 2)()
+    assert lib.vdit_pipeline_default_groups(24, ctypes.cast(buf, ctypes.c_void_p), 2) == 0
+    assert lib.vdit_pipeline_default_groups(0, ctypes.cast(buf, ctypes.c_void_p), 2) == 0
