@@ -193,15 +193,18 @@ def test_full_size_forced_online_720p():
     _full_size_check(configs.SR720, "online", per_frame_random=4)
 
 
-def test_full_size_dense_sweep_large_key_offset():
-    """Dense sweep point with key offsets of scale 2 and 6 outlier heads: the
-    mean term q.c of the bound is large (centring keeps the 18 regular heads
-    eligible, the outliers take the online path), over a key count that is not
-    a multiple of 16."""
-    w = {x.name: x for x in configs.dense_sweep()}["dense_s2_out6"]
-    st = _full_size_check(w, "auto", per_frame_random=3)
+@pytest.mark.parametrize("w", configs.dense_sweep(), ids=lambda w: w.name)
+def test_full_size_dense_sweep(w):
+    """Every point of the dense base-DiT eligibility sweep (key offset scale s in
+    {0, 0.5, 2} x 0, 1 or 6 of 24 outlier heads) at full size, AUTO mode as
+    timed: attention on a light stratified row sample over a key count that is
+    not a multiple of 16, and exactly the outlier heads on the online path
+    (centring keeps every regular head eligible at every offset scale; at s = 2
+    the mean term q.c of the bound is large)."""
+    st = _full_size_check(w, "auto", per_frame_random=2)
     elig = st["eligible"].cpu().numpy().reshape(-1)
-    assert elig[:18].all() and not elig[18:].any()
+    want = np.array([0 if h in w.outlier_heads else 1 for h in range(w.H)], dtype=elig.dtype)
+    assert np.array_equal(elig, want), (w.name, elig)
 
 
 def test_batch_of_two_at_720p_geometry():

@@ -20,7 +20,7 @@ def run(w, q, k):
     return {k_: v.cpu() for k_, v in st.items()}
 
 
-@pytest.mark.parametrize("w", configs.ALL + tuple(configs.dense_sweep()[::4]), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", configs.ALL + tuple(configs.dense_sweep()), ids=lambda w: w.name)
 def test_key_stats_parity(w):
     q, k, _ = synth.make_qkv(w)
     got = run(w, q, k)
@@ -34,6 +34,10 @@ def test_key_stats_parity(w):
     assert np.array_equal(got["eligible"].numpy(), want["elig"])
     # margins: eligibility is decided far from the threshold on these workloads
     assert (np.abs(want["G"] - TAU) > 1e-3 * TAU).all()
+    # exactly the outlier heads fall back: with centred keys the per-head key
+    # offset (any scale in the dense sweep) leaves every regular head eligible
+    for h in range(w.H):
+        assert (got["eligible"][:, h] == (0 if h in w.outlier_heads else 1)).all(), (w.name, h)
 
 
 def test_key_stats_deterministic_and_strided():

@@ -6,7 +6,11 @@ pay cudaMalloc's implicit synchronisation): its scratch is a fixed array inside
 the library. These tests call it through the C ABI and compare it with
 vdit_key_stats (caller-provided workspace) on two calls in a row with different
 inputs and sizes, so state left in the shared array by the first call cannot
-leak into the second. This file is collected last on purpose.
+leak into the second. Both entry points run the same kernels in the same fixed
+reduction order, so their results must be equal bit for bit; each result is also
+checked against the fp64 oracle (relative 1e-5, eligibility exact), so a fault
+that corrupted both the same way would still fail. This file is collected last
+on purpose.
 """
 import ctypes
 
@@ -16,6 +20,8 @@ import torch
 
 import block_sparse_video_frame_gb300 as vd
 from block_sparse_video_frame_gb300 import _build, configs, synth
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -51,10 +57,18 @@ def _noalloc(lib, q, k, scale, tau=64.0):
 
 
 def _compare(got, want):
-    for key in ("k_mean", "k_rmax", "q_nmax", "gap"):
-        np.testing.assert_allclose(got[key].cpu().numpy(), want[key].cpu().numpy(),
-                                   rtol=1e-5, atol=1e-6, err_msg=key)
-    assert torch.equal(got["eligible"], want["eligible"])
+    """Bitwise equality with the workspace entry point."""
+    for key in ("k_mean", "k_rmax", "q_nmax", "gap", "eligible"):
+        assert torch.equal(got[key], want[key]), key
+
+
+def _against_oracle(got, q, k, scale, tau=64.0):
+    ref = oracle.key_stats(q.cpu(), k.cpu(), scale, tau)
+    c = ref["c"]
+    assert np.abs(got["k_mean"].double().cpu().numpy() - c).max() <= 1e-5 * np.abs(c).max() + 1e-6
+    for key, rk in (("k_rmax", "R"), ("q_nmax", "qmax"), ("gap", "G")):
+        np.testing.assert_allclose(got[key].double().cpu().numpy(), ref[rk], rtol=1e-5, err_msg=key)
+    assert np.array_equal(got["eligible"].cpu().numpy(), ref["elig"])
 
 
 def test_noalloc_matches_workspace_version_two_calls():
@@ -66,6 +80,7 @@ def test_noalloc_matches_workspace_version_two_calls():
         want = vd.key_stats(q, k, w.scale)
         torch.cuda.synchronize()
         _compare(got, want)
+        _against_oracle(got, q, k, w.scale)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
