@@ -66,6 +66,10 @@ def parse_args(argv=None):
     ap.add_argument("--bs-sweep", action="store_true",
                     help="schedule block size sweep on one workload: plan build time, CSR size and "
                          "attention time per valid block size; one JSON line each")
+    ap.add_argument("--ablation", action="store_true",
+                    help="time the design before frame alignment (frame-blind 128-multiple tiles "
+                         "with mask predicates; window and reference frame as two passes and a "
+                         "merge) against the frame-aligned single pass, one line per form")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the one-line contract: time the attention call on every "
                          "workload and the dense eligibility sweep in AUTO, ONLINE and STATIC "
@@ -360,6 +364,71 @@ def config_of(w, args):
             "l2": "no flush: Q+K+V inputs are larger than the 126 MB L2"}
 
 
+def run_ablation(args):
+    """The pages' design before frame alignment ("Deleting the Mask", Fig. 3) on
+    this GPU, as forms of the same library, against the frame-aligned single
+    pass: frame-blind 128-multiple tiles with mask predicates on straddling tiles
+    (sequence padded to a multiple of 128); the window and the reference frame as
+    two passes writing fp32 intermediates that a merge kernel re-reads (with
+    frame-aligned or frame-blind tiles). Every form computes the same attention
+    (tests/test_gpu_ablation.py); the effective rate counts the live pairs only.
+    Forms are timed in rotated rounds, each form's median round reported."""
+    import torch
+    import block_sparse_video_frame_gb300 as vd
+    from block_sparse_video_frame_gb300 import configs, synth
+    torch.cuda.set_device(0)
+    vd.load_library()
+    w = configs.BY_NAME[args.workload]
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    st = vd.key_stats(q, k, w.scale)
+    flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=q.device)
+    forms = {"frame_aligned": lambda: vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, out=o,
+                                                  lse=lse, check=False),
+             "tiles128": lambda: vd.attn_fwd_tiles128(plan, q, k, v, st, w.scale, mode=args.mode, out=o,
+                                                      lse=lse, check=False)}
+    two = w.ref >= 0 and not w.dense
+    if two:
+        pw = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size, part="window")
+        pr = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size, part="reference")
+        wsb = torch.empty(vd.two_pass_workspace_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8, device=q.device)
+        for tiles in ("frame", "128"):
+            forms[f"two_pass_{tiles}"] = (lambda t=tiles: vd.attn_fwd_two_pass(
+                pw, pr, q, k, v, st, w.scale, mode=args.mode, tiles=t, out=o, lse=lse, workspace=wsb,
+                check=False))
+    names = list(forms)
+    rounds = {n: [] for n in names}
+    for rnd in range(3):
+        for i in range(len(names)):
+            name = names[(i + rnd) % len(names)]
+            for _ in range(3):
+                forms[name]()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 10
+            e0.record()
+            for _ in range(n):
+                forms[name]()
+            e1.record()
+            torch.cuda.synchronize()
+            for pl in [plan] + ([pw, pr] if two else []):
+                if pl.status() != 0:
+                    raise RuntimeError(f"expired wait in {w.name} {name}")
+            rounds[name].append(e0.elapsed_time(e1) / n)
+    base = statistics.median(rounds["frame_aligned"])
+    full, partial, dead = plan.block_census(128)
+    for name in names:
+        ms = statistics.median(rounds[name])
+        print(json.dumps({"workload": w.name, "form": name, "mode": args.mode, "ms_per_call": ms,
+                          "ms_rounds": rounds[name], "tflops": flops / (ms * 1e-3) / 1e12,
+                          "of_frame_aligned": base / ms,
+                          "partial_of_live_blocks_at_128": partial / (full + partial),
+                          "live_pairs_per_head": plan.live_pairs}), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """Attention-call timing per workload and softmax mode (static bound vs
     online), with each head's eligibility: the dense base-DiT sweep reports what
@@ -390,13 +459,13 @@ def run_sweep(args):
                 stats = stf if mode == "auto_framed" else st
                 md = "auto" if mode == "auto_framed" else mode
                 for _ in range(3):
-                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
+                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse, check=False)
                 torch.cuda.synchronize()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 n = 10
                 e0.record()
                 for _ in range(n):
-                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse)
+                    vd.attn_fwd(plan, q, k, v, stats, w.scale, mode=md, out=o, lse=lse, check=False)
                 e1.record()
                 torch.cuda.synchronize()
                 if plan.status() != 0:
@@ -505,7 +574,7 @@ def run_bs_sweep(args):
     for bs in sizes:
         plan = vd.attn_plan(w.F, w.T, w.W, w.ref, bs)
         plan_ms = timed(lambda: plan.rebuild(), 20)
-        attn_ms = timed(lambda: vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False), 10)
+        attn_ms = timed(lambda: vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False, check=False), 10)
         if plan.status() != 0:
             raise RuntimeError(f"expired wait at bs={bs}")
         flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
@@ -573,7 +642,7 @@ def run_pipeline_sweep(args):
         "both_directions_total": link_gbs([(q, q_h), (o_h, o)])},
         "bytes_per_tensor": q_h.numel() * q_h.element_size()}), flush=True)
     dev_ms = timed(lambda: (vd.key_stats(q, k, w.scale, out=st),
-                            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False)), n)
+                            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, with_lse=False, check=False)), n)
     moved = 4 * q_h.numel() * q_h.element_size()
     specs = [g for g in (1, 2, 3, 4, 6, 8, 12, 24) if g <= w.H] + [0]
     if w.H == 24:   # tapered: small first and last groups shorten the exposed ends
@@ -581,7 +650,7 @@ def run_pipeline_sweep(args):
                   [1, 2, 3, 3, 3, 3, 3, 3, 2, 1]]
     for g in specs:
         pipe = vd.Pipeline(plan, w.B, w.H, w.D, g)
-        ms = timed(lambda: pipe.run(q_h, k_h, v_h, o_h, w.scale), n)
+        ms = timed(lambda: pipe.run(q_h, k_h, v_h, o_h, w.scale, check=False), n)
         pipe.close()
         if plan.status() != 0:
             raise RuntimeError(f"expired wait with {g} groups")
@@ -608,7 +677,7 @@ def run_sustained(args):
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
     plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
     st = vd.key_stats(q, k, w.scale)
-    o, lse = vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode)
+    o, lse = vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, check=False)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     burst = 20
@@ -616,7 +685,7 @@ def run_sustained(args):
     t0 = time.time()
     while time.time() - t0 < 0.5 * args.sustained:
         for _ in range(burst):
-            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode)
+            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode, check=False)
         torch.cuda.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
@@ -626,7 +695,7 @@ def run_sustained(args):
     a.record(stream)
     while time.time() - t0 < args.sustained:
         for _ in range(burst):
-            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode)
+            vd.attn_fwd(plan, q, k, v, st, w.scale, out=o, lse=lse, mode=args.mode, check=False)
         n += burst
         torch.cuda.synchronize()
     b.record(stream)
@@ -651,6 +720,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.ablation:
+        return run_ablation(args)
     if args.prologue:
         return run_prologue(args)
     if args.pipeline_sweep:
@@ -681,6 +752,14 @@ def main(argv=None):
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
     flops = 4.0 * w.D * plan.live_pairs * w.B * w.H
+    # partial blocks under frame-blind tilings ("Deleting the Mask": about one live
+    # block in five partial), counted on the device before the timed region
+    census = {}
+    for tile in (128, 1024):
+        full, partial, dead = plan.block_census(tile)
+        census[f"tile_{tile}"] = {"full": full, "partial": partial, "dead": dead,
+                                  "partial_of_live": partial / max(1, full + partial)}
+    census["tile_bs"] = dict(zip(("full", "partial", "dead"), plan.block_census(w.block_size)))
     framed = args.bound == "frame"
     if framed:
         st = vd.key_stats_framed(plan, q, k, w.scale)
@@ -704,7 +783,7 @@ def main(argv=None):
         stats(q, k)
         if ev_a is not None:
             ev_a.record(stream)
-        vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, out=o, lse=lse)
+        vd.attn_fwd(plan, q, k, v, st, w.scale, mode=args.mode, out=o, lse=lse, check=False)
         if ev_b is not None:
             ev_b.record(stream)
 
@@ -761,7 +840,7 @@ def main(argv=None):
 
             def e2e_step():
                 plan.rebuild()
-                pipe.run(q_h, k_h, v_h, o_h, w.scale, mode=args.mode)
+                pipe.run(q_h, k_h, v_h, o_h, w.scale, mode=args.mode, check=False)
         else:
             qe, ke, ve = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
@@ -769,7 +848,7 @@ def main(argv=None):
                 qe.copy_(q_h, non_blocking=True); ke.copy_(k_h, non_blocking=True); ve.copy_(v_h, non_blocking=True)
                 plan.rebuild()
                 stats(qe, ke)
-                vd.attn_fwd(plan, qe, ke, ve, st, w.scale, mode=args.mode, out=o, lse=lse)
+                vd.attn_fwd(plan, qe, ke, ve, st, w.scale, mode=args.mode, out=o, lse=lse, check=False)
                 o_h.copy_(o, non_blocking=True)
         for _ in range(2):
             e2e_step()
@@ -812,7 +891,7 @@ def main(argv=None):
                 for i in range(n):
                     j = i % 2
                     plans_e[j].rebuild(stream=side[j])
-                    pipes[j].run(q_h, k_h, v_h, outs_h[j], w.scale, mode=args.mode, stream=side[j])
+                    pipes[j].run(q_h, k_h, v_h, outs_h[j], w.scale, mode=args.mode, stream=side[j], check=False)
                 for sd in side:
                     stream.wait_stream(sd)
                 b.record(stream)
@@ -849,7 +928,7 @@ def main(argv=None):
                 with torch.cuda.stream(side[j]):
                     plans2[j].rebuild()
                     vd.key_stats(q, k, w.scale, workspace=ws2[j], out=st2[j])
-                    vd.attn_fwd(plans2[j], q, k, v, st2[j], w.scale, mode=args.mode, out=o2[j], lse=l2[j])
+                    vd.attn_fwd(plans2[j], q, k, v, st2[j], w.scale, mode=args.mode, out=o2[j], lse=l2[j], check=False)
             for sd in side:
                 stream.wait_stream(sd)
             b.record(stream)
@@ -878,17 +957,19 @@ def main(argv=None):
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V, per-head key offsets, x20 outlier keys)",
-            "config": dict(config_of(w, args), live_pairs_per_head=plan.live_pairs,
-                           flop_per_step_per_gpu=flops,
-                           pct_of_2250_tflops=100.0 * value / ws / NOMINAL_BF16_TFLOPS,
-                           attn_ms_median=statistics.median(attn_ms),
-                           attn_ms_min=min(attn_ms), attn_ms_max=max(attn_ms)),
+            "config": config_of(w, args),
+            "live_pairs_per_head": plan.live_pairs,
+            "flop_per_step_per_gpu": flops,
+            "pct_of_2250_tflops": 100.0 * value / ws / NOMINAL_BF16_TFLOPS,
+            "attn_ms": {"mean": statistics.mean(attn_ms), "median": statistics.median(attn_ms),
+                        "min": min(attn_ms), "max": max(attn_ms)},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "traffic": (args.traffic_bytes if args.traffic_bytes is not None
                                      else recorded_traffic(w.name)),
                          "kernel": f"attn_fwd_kernel<{w.D}>", "peak_source":
                          f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
+            "block_census": census,
             "gpu_launches": LAUNCHES_PER_STEP * args.steps,
             "clocks": clocks,
         }

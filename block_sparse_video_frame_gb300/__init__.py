@@ -32,7 +32,11 @@ EXPORTED = ("vdit_attn_plan", "vdit_plan_rebuild", "vdit_plan_get_info", "vdit_p
             "vdit_key_stats_framed", "vdit_attn_fwd_framed", "vdit_qkv_fold_gamma",
             "vdit_rope_table", "vdit_qkv_workspace_size", "vdit_qkv_prologue", "vdit_qkv_status",
             "vdit_pipeline_create", "vdit_pipeline_run", "vdit_pipeline_destroy",
-            "vdit_pipeline_default_groups", "vdit_set_alloc_fail_after")
+            "vdit_pipeline_default_groups", "vdit_set_alloc_fail_after",
+            "vdit_set_launch_fail_after", "vdit_plan_block_census", "vdit_attn_plan_part",
+            "vdit_attn_fwd_tiles128", "vdit_attn_two_pass_workspace_size", "vdit_attn_fwd_two_pass")
+PARTS = {"all": 0, "window": 1, "reference": 2}
+TILES = {"frame": 0, "128": 1}
 
 
 class VditError(RuntimeError):
@@ -51,7 +55,8 @@ class PlanInfo(ctypes.Structure):
                 ("n_classes", ctypes.c_int32),
                 ("d_row_ptr", ctypes.c_void_p), ("d_col_idx", ctypes.c_void_p),
                 ("d_frame_runs", ctypes.c_void_p), ("d_segments", ctypes.c_void_p),
-                ("d_units", ctypes.c_void_p), ("d_class_off", ctypes.c_void_p)]
+                ("d_units", ctypes.c_void_p), ("d_class_off", ctypes.c_void_p),
+                ("part", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -119,6 +124,20 @@ def load_library(path: str = LIB_PATH):
         lib.vdit_pipeline_default_groups.restype = i32
         lib.vdit_set_alloc_fail_after.argtypes = [i32]
         lib.vdit_set_alloc_fail_after.restype = None
+        lib.vdit_attn_plan_part.argtypes = [i32, i32, i32, i32, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.vdit_attn_plan_part.restype = ctypes.c_int
+        lib.vdit_attn_fwd_tiles128.argtypes = list(lib.vdit_attn_fwd.argtypes)
+        lib.vdit_attn_fwd_tiles128.restype = ctypes.c_int
+        lib.vdit_attn_two_pass_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.vdit_attn_two_pass_workspace_size.restype = ctypes.c_size_t
+        lib.vdit_attn_fwd_two_pass.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, _I64x3,
+                                               _I64x3, _I64x3, _I64x3, f32, vp, vp, vp, i32, i32, vp,
+                                               ctypes.c_size_t, vp]
+        lib.vdit_attn_fwd_two_pass.restype = ctypes.c_int
+        lib.vdit_plan_block_census.argtypes = [vp, i32, vp, vp]
+        lib.vdit_plan_block_census.restype = ctypes.c_int
+        lib.vdit_set_launch_fail_after.argtypes = [i32]
+        lib.vdit_set_launch_fail_after.restype = None
         _lib = lib
         return lib
 
@@ -158,11 +177,16 @@ def _check_bhnd(name, t, D=None):
 class Plan:
     """Owns a vdit_plan (device block schedule + work units)."""
 
-    def __init__(self, F, T, W, ref, block_size, stream=None):
+    def __init__(self, F, T, W, ref, block_size, stream=None, part="all"):
         lib = load_library()
         h = ctypes.c_void_p()
-        _check(lib.vdit_attn_plan(int(F), int(T), int(W), int(ref), int(block_size),
-                                  _stream(stream), ctypes.byref(h)))
+        pt = PARTS[part] if isinstance(part, str) else int(part)
+        if pt == 0:
+            _check(lib.vdit_attn_plan(int(F), int(T), int(W), int(ref), int(block_size),
+                                      _stream(stream), ctypes.byref(h)))
+        else:
+            _check(lib.vdit_attn_plan_part(int(F), int(T), int(W), int(ref), int(block_size), pt,
+                                           _stream(stream), ctypes.byref(h)))
         self._h = h
         self.info = PlanInfo()
         _check(lib.vdit_plan_get_info(h, ctypes.byref(self.info)))
@@ -188,6 +212,23 @@ class Plan:
         if st not in (VDIT_OK, VDIT_ERR_TIMEOUT):
             _check(st)
         return int(code.value)
+
+    def block_census(self, tile, stream=None):
+        """(full, partial, dead) counts of tile x tile blocks over the N x N token
+        pairs, computed on the device (vdit_plan_block_census); synchronises."""
+        import torch
+        counts = torch.empty(3, dtype=torch.int64, device="cuda")
+        _check(load_library().vdit_plan_block_census(self._h, int(tile), _ptr(counts), _stream(stream)))
+        return tuple(int(x) for x in counts.cpu().tolist())
+
+    def check(self, stream=None):
+        """Synchronise the stream and raise VditError(VDIT_ERR_TIMEOUT) when a kernel
+        launched with this plan gave up on an expired wait (its output is then
+        incomplete); the status word is cleared either way."""
+        code = self.status(stream)
+        if code != 0:
+            raise VditError(VDIT_ERR_TIMEOUT, f"a kernel's bounded wait expired (site code {code}); "
+                                              "its output is incomplete")
 
     def _device_array(self, ptr, n):
         """Copy of n int32 values of plan-owned device memory (zero-copy view via
@@ -237,9 +278,10 @@ class _DeviceInts:
                                          "strides": None}
 
 
-def attn_plan(F, T, W, ref, block_size, stream=None) -> Plan:
-    """Block schedule of the frame-window + reference-frame mask (vdit_attn_plan)."""
-    return Plan(F, T, W, ref, block_size, stream)
+def attn_plan(F, T, W, ref, block_size, stream=None, part="all") -> Plan:
+    """Block schedule of the frame-window + reference-frame mask (vdit_attn_plan),
+    or of one part of it: "window" or "reference" (vdit_attn_plan_part)."""
+    return Plan(F, T, W, ref, block_size, stream, part)
 
 
 def key_stats(q, k, scale, tau=64.0, stream=None, workspace=None, out=None):
@@ -317,9 +359,8 @@ def key_stats_workspace_bytes(B, H, N, D) -> int:
     return int(load_library().vdit_key_stats_workspace_size(int(B), int(H), int(N), int(D)))
 
 
-def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype=None,
-             with_lse=True, out=None, lse=None, stream=None):
-    """Fused block-sparse attention (vdit_attn_fwd). Returns (o, lse or None)."""
+def _attn_args(plan, q, k, v, stats, scale, mode, out_dtype, with_lse, out, lse):
+    """Validated arguments shared by the attention calls."""
     import torch
     _check_bhnd("q", q)
     D = q.shape[3]
@@ -350,11 +391,77 @@ def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype
     if stats is not None:
         km = stats["k_mean"]
         kr, el = (stats["seg_rmax"], stats["seg_eligible"]) if framed else (stats["k_rmax"], stats["eligible"])
-    fn = load_library().vdit_attn_fwd_framed if framed else load_library().vdit_attn_fwd
-    _check(fn(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), o_code, _ptr(lse), B, H, D,
-              _strides(q), _strides(k), _strides(v), _strides(out), float(scale), _ptr(km), _ptr(kr),
-              _ptr(el), m, _stream(stream)))
-    return out, lse
+    return dict(B=B, H=H, N=N, D=D, scale=float(scale), m=m, out=out, o_code=o_code, lse=lse,
+                km=km, kr=kr, el=el, framed=framed)
+
+
+def attn_fwd(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype=None,
+             with_lse=True, out=None, lse=None, stream=None, check=True):
+    """Fused block-sparse attention (vdit_attn_fwd). Returns (o, lse or None).
+
+    With check=True (the default) the call synchronises the stream and raises
+    VditError(VDIT_ERR_TIMEOUT) if the kernel gave up on an expired wait, so an
+    incomplete O is never returned silently. check=False keeps the call
+    asynchronous; the caller then checks with plan.check() (or plan.status())
+    once the stream has passed the call."""
+    a = _attn_args(plan, q, k, v, stats, scale, mode, out_dtype, with_lse, out, lse)
+    lib = load_library()
+    fn = lib.vdit_attn_fwd_framed if a["framed"] else lib.vdit_attn_fwd
+    _check(fn(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(a["out"]), a["o_code"], _ptr(a["lse"]),
+              a["B"], a["H"], a["D"], _strides(q), _strides(k), _strides(v), _strides(a["out"]),
+              a["scale"], _ptr(a["km"]), _ptr(a["kr"]), _ptr(a["el"]), a["m"], _stream(stream)))
+    if check:
+        plan.check(stream)
+    return a["out"], a["lse"]
+
+
+def attn_fwd_tiles128(plan: Plan, q, k, v, stats=None, scale=None, mode="auto", out_dtype=None,
+                      with_lse=True, out=None, lse=None, stream=None, check=True):
+    """The attention with the frame-blind tiling of the design before frame
+    alignment ("Deleting the Mask", Fig. 3): 128-multiple tiles over the padded
+    sequence, mask predicates on straddling tiles (vdit_attn_fwd_tiles128).
+    Same results as attn_fwd; an ablation. Per-head statistics only."""
+    a = _attn_args(plan, q, k, v, stats, scale, mode, out_dtype, with_lse, out, lse)
+    if a["framed"]:
+        raise ValueError("the frame-blind tiling takes the per-head statistics (key_stats)")
+    _check(load_library().vdit_attn_fwd_tiles128(
+        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(a["out"]), a["o_code"], _ptr(a["lse"]), a["B"],
+        a["H"], a["D"], _strides(q), _strides(k), _strides(v), _strides(a["out"]), a["scale"],
+        _ptr(a["km"]), _ptr(a["kr"]), _ptr(a["el"]), a["m"], _stream(stream)))
+    if check:
+        plan.check(stream)
+    return a["out"], a["lse"]
+
+
+def two_pass_workspace_bytes(B, H, N, D) -> int:
+    return int(load_library().vdit_attn_two_pass_workspace_size(int(B), int(H), int(N), int(D)))
+
+
+def attn_fwd_two_pass(plan_window: Plan, plan_reference: Plan, q, k, v, stats=None, scale=None,
+                      mode="auto", tiles="frame", out_dtype=None, with_lse=True, out=None, lse=None,
+                      workspace=None, stream=None, check=True):
+    """The attention as the window pass, the reference-frame pass and a merge of
+    their fp32 intermediates (vdit_attn_fwd_two_pass), the design before frame
+    alignment ("Deleting the Mask"). plan_window / plan_reference: attn_plan(...,
+    part="window" / "reference") of one mask. tiles: "frame" (frame-aligned
+    passes) or "128" (frame-blind tiling). Same results as attn_fwd; an ablation."""
+    import torch
+    a = _attn_args(plan_window, q, k, v, stats, scale, mode, out_dtype, with_lse, out, lse)
+    if a["framed"]:
+        raise ValueError("the two-pass form takes the per-head statistics (key_stats)")
+    need = two_pass_workspace_bytes(a["B"], a["H"], a["N"], a["D"])
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(load_library().vdit_attn_fwd_two_pass(
+        plan_window.handle, plan_reference.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(a["out"]),
+        a["o_code"], _ptr(a["lse"]), a["B"], a["H"], a["D"], _strides(q), _strides(k), _strides(v),
+        _strides(a["out"]), a["scale"], _ptr(a["km"]), _ptr(a["kr"]), _ptr(a["el"]), a["m"],
+        TILES[str(tiles)], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    if check:
+        plan_window.check(stream)
+        plan_reference.check(stream)
+    return a["out"], a["lse"]
 
 
 def fold_gamma(w, gamma, out=None, stream=None):
@@ -449,12 +556,18 @@ class Pipeline:
         # event recorded after the run: they stay referenced until it completes
         self._inflight = []
 
-    def run(self, q_h, k_h, v_h, o_h, scale, lse_h=None, tau=64.0, mode="auto", stream=None):
+    def run(self, q_h, k_h, v_h, o_h, scale, lse_h=None, tau=64.0, mode="auto", stream=None,
+            check=True):
         """q_h, k_h, v_h, o_h: bf16 CPU tensors (pinned for overlap) indexed
         [B, H, N, D] with identical strides and d contiguous; lse_h: optional fp32
-        [B, H, N] contiguous CPU tensor. Asynchronous: synchronise the stream
-        before reading o_h. The host tensors stay referenced by the pipeline until
-        the run's copies have completed."""
+        [B, H, N] contiguous CPU tensor. The host tensors stay referenced by the
+        pipeline until the run's copies have completed.
+
+        With check=True (the default) the call synchronises the stream, so o_h is
+        complete on return, and raises VditError(VDIT_ERR_TIMEOUT) if any of the
+        run's attention kernels gave up on an expired wait. check=False keeps the
+        run asynchronous: synchronise the stream before reading o_h, and call
+        self.plan.check() to learn of expired waits."""
         import torch
         self._inflight = [(ev, held) for ev, held in self._inflight if not ev.query()]
         ts = (q_h, k_h, v_h, o_h)
@@ -476,6 +589,8 @@ class Pipeline:
         ev.record(stream if stream is not None else torch.cuda.current_stream())
         self._inflight.append((ev, (q_h, k_h, v_h, o_h, lse_h)))
         _check(status)
+        if check:
+            self.plan.check(stream)
         return o_h
 
     def close(self):
@@ -505,6 +620,13 @@ def set_alloc_fail_after(n: int) -> None:
     """Test hook: the n-th device allocation the library makes from now on fails
     once (VDIT_ERR_NOMEM); n <= 0 switches it off (vdit_set_alloc_fail_after)."""
     load_library().vdit_set_alloc_fail_after(int(n))
+
+
+def set_launch_fail_after(n: int) -> None:
+    """Test hook: the n-th attention launch from now on is refused once, as if
+    the launch had failed (VDIT_ERR_CUDA); n <= 0 switches it off
+    (vdit_set_launch_fail_after)."""
+    load_library().vdit_set_launch_fail_after(int(n))
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -32,6 +32,19 @@ cudaError_t device_alloc(void **ptr, size_t bytes) {
     return cudaMalloc(ptr, bytes);
 }
 
+namespace {
+std::atomic<int> g_launch_fail_after{0};   // > 0: attention launches left until the one that fails
+}
+
+bool launch_fails_by_hook() {
+    int n = g_launch_fail_after.load(std::memory_order_relaxed);
+    while (n > 0) {
+        if (g_launch_fail_after.compare_exchange_weak(n, n - 1, std::memory_order_relaxed))
+            return n == 1;
+    }
+    return false;
+}
+
 void set_error(const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -56,6 +69,10 @@ extern "C" void vdit_set_wait_limit_ns(uint64_t ns) {
 
 extern "C" void vdit_set_alloc_fail_after(int32_t n) {
     vdit::g_fail_after.store(n > 0 ? n : 0, std::memory_order_relaxed);
+}
+
+extern "C" void vdit_set_launch_fail_after(int32_t n) {
+    vdit::g_launch_fail_after.store(n > 0 ? n : 0, std::memory_order_relaxed);
 }
 
 extern "C" const char *vdit_version(void) { return "libvdit 0.1 (sm_103a, tcgen05)"; }

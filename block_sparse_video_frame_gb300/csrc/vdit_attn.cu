@@ -29,10 +29,11 @@
 // so one warpgroup's exponentials overlap the other's MMAs. TMEM (512 cols):
 // O0 | O1 | S0 | S1; P (bf16, two per 32-bit column) overwrites the first half
 // of its S buffer and is the A operand (from TMEM) of the P.V MMA.
-// A segment with an odd number of tiles ends in a lone tile. On the static path
-// its key tiles alternate between both slots (both read the same Q tile), so
-// it overlaps like a pair; the epilogue adds O0 + O1 and the two row sums,
-// exact because both halves share the static bound.
+// A segment with an odd number of tiles ends in a lone tile. Its key tiles
+// alternate between both slots (both read the same Q tile), so it overlaps like
+// a pair; the epilogue adds O0 + O1 and the two row sums, exact because both
+// halves share the static bound (online: both halves rescaled to the larger of
+// their two running maxima first).
 // Every wait is bounded in time; on expiry the CTA records a site code in the
 // plan's status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -60,18 +61,6 @@ constexpr int kWarpSoftmax0 = 2;      // softmax warpgroups: warps 2-5 and 6-9
 constexpr int kHalfBytes = 128 * 128; // 128 rows x 64 bf16 (one swizzle-atom column)
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr float kLazyRescale = 8.0f;  // online: rescale only when the max rises > 2^8
-// Of every 8 columns of S, this many take their exponential on the FMA pipe
-// (exp2_fma) instead of MUFU ex2. Zero: MUFU ex2 issues at about 4 clk per warp
-// instruction, which does not limit the softmax, while the polynomial costs about
-// 9 FMA-pipe issue slots; every non-zero share measured slower.
-constexpr int kPolyPer8 = 0;
-
-template <int C>
-__device__ __forceinline__ float softmax_exp2(float x) {
-    if constexpr ((C % 8) >= 8 - kPolyPer8) return exp2_fma(x);
-    else return ex2(x);
-}
-
 // Compile-time loop: f(std::integral_constant<int, i>) for i in [0, N).
 template <int N, int I = 0, typename F>
 __device__ __forceinline__ void static_for(F &&f) {
@@ -94,8 +83,8 @@ struct Layout {
     static constexpr int kK = kQ + kTilesPerUnit * kTileBytes;
     static constexpr int kV = kK + kStagesK * kTileBytes;
     static constexpr int kBar = kV + kStagesV * kTileBytes;
-    static constexpr int kX = kBar + 256;          // row sums handed between warpgroups
-    static constexpr int kBytes = kX + kTileRows * 4;
+    static constexpr int kX = kBar + 256;          // row sums and maxima handed between warpgroups
+    static constexpr int kBytes = kX + kTileRows * 8;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static constexpr uint32_t kTmemO = 0;         // O0 at col 0, O1 at col D
     static constexpr uint32_t kTmemS = 2 * D;     // S0 at 2D, S1 at 2D + 128
@@ -130,6 +119,10 @@ struct Params {
     int mode;
     int *status;
     unsigned long long timeout_ns;
+    // frame-blind tiling (ablation of the design before frame alignment): the
+    // mask's geometry, which part of it runs, and the 256-row query blocks per head
+    int F, T, W, ref, part;
+    int n_blocks;
 };
 
 struct Work {
@@ -183,11 +176,85 @@ __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
     u.stat = p.mode == VDIT_MODE_FORCE_STATIC ||
              (p.mode == VDIT_MODE_AUTO &&
               (p.seg_elig ? p.seg_elig[(size_t)u.bh * p.nseg + u.seg] : p.elig[u.bh]) != 0);
-    // A lone tile has no partner to overlap its softmax with. On the static path
-    // its key tiles alternate between both slots (even ones in slot 0, odd ones
-    // in slot 1, both reading the same Q tile): the bound is common to both
-    // halves, so O = O0 + O1 and l = l0 + l1 exactly, with no rescale.
-    u.alt = u.nact == 1 && u.nkt >= 2 && u.stat;
+    // A lone tile has no partner to overlap its softmax with. Its key tiles
+    // alternate between both slots (even ones in slot 0, odd ones in slot 1, both
+    // reading the same Q tile). On the static path the bound is common to both
+    // halves, so O = O0 + O1 and l = l0 + l1 exactly, with no rescale; online,
+    // each half keeps its own running max and the epilogue rescales both halves
+    // to the larger one.
+    u.alt = u.nact == 1 && u.nkt >= 2;
+}
+
+// The design before frame alignment ("Deleting the Mask", Fig. 3): query blocks
+// of 256 rows (two 128-row tiles) and 128-key tiles at fixed multiples of 128
+// over the sequence padded to a multiple of 128, blind to frame boundaries. A
+// block visits every 128-key tile that holds a live key of one of its rows: the
+// window of its first to last frame and, when some row's window leaves it out,
+// the reference frame (each rounded out to 128 keys); tiles where a row also
+// sees dead keys are masked element by element in the softmax. Row i of the
+// padded tail (i >= N) is computed as a row of the last frame and not stored.
+// Blocks walk the heads two at a time in sequence order.
+__device__ __forceinline__ void decode_tiled(const Params &p, long long w, Work &u) {
+    const int BH = p.B * p.H;
+    const long long per_head = p.n_blocks;
+    const long long g = w / (per_head * kHeadGroup);
+    const int gh = min(kHeadGroup, BH - (int)g * kHeadGroup);
+    w -= g * per_head * kHeadGroup;
+    u.bh = (int)(g * kHeadGroup + w / per_head);
+    const int blk = (int)(w % per_head);
+    u.b = u.bh / p.H;
+    u.h = u.bh % p.H;
+    (void)gh;
+    const int npad = (p.N + kBK - 1) / kBK * kBK;
+    u.seg = 0;
+    u.pair = 0;
+    u.row0 = blk * kTilesPerUnit * kTileRows;
+    u.rows = min(kTilesPerUnit * kTileRows, npad - u.row0);
+    u.ntile = u.rows / kTileRows;
+    u.nact = u.ntile;
+    const int T = p.T;
+    const int fa = u.row0 / T, fb = (min(u.row0 + u.rows, p.N) - 1) / T;
+    const int wlo = max(0, fa - p.W), whi = min(p.F - 1, fb + p.W);
+    // some row of the block has the reference frame outside its window
+    const bool ref_needed = p.ref >= 0 && (p.ref < fb - p.W || p.ref > fa + p.W);
+    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+    if (p.part != VDIT_PART_REFERENCE) { lo0 = wlo * T; hi0 = (whi + 1) * T; }
+    if (p.part != VDIT_PART_WINDOW && ref_needed && (p.part == VDIT_PART_REFERENCE || p.ref < wlo || p.ref > whi)) {
+        lo1 = p.ref * T;
+        hi1 = (p.ref + 1) * T;
+    }
+    auto round_out = [&](int &lo, int &hi) {
+        if (hi > lo) { lo = lo / kBK * kBK; hi = min((hi + kBK - 1) / kBK * kBK, npad); }
+    };
+    round_out(lo0, hi0);
+    round_out(lo1, hi1);
+    if (hi0 <= lo0) { lo0 = lo1; hi0 = hi1; lo1 = hi1 = 0; }          // the reference run alone
+    if (hi1 > lo1) {
+        if (lo1 < lo0) { int t0 = lo0, t1 = hi0; lo0 = lo1; hi0 = hi1; lo1 = t0; hi1 = t1; }
+        if (lo1 <= hi0) { hi0 = max(hi0, hi1); lo1 = hi1 = 0; }        // overlapping after rounding
+    }
+    u.lo0 = lo0; u.hi0 = hi0; u.lo1 = lo1; u.hi1 = hi1;
+    u.nt0 = (hi0 - lo0) / kBK;
+    u.nkt = u.nt0 + (hi1 - lo1) / kBK;
+    u.stat = p.mode == VDIT_MODE_FORCE_STATIC || (p.mode == VDIT_MODE_AUTO && p.elig[u.bh] != 0);
+    u.alt = u.nact == 1 && u.nkt >= 2;
+}
+
+template <bool kTiled>
+__device__ __forceinline__ void decode_any(const Params &p, long long w, Work &u) {
+    if constexpr (kTiled) decode_tiled(p, w, u);
+    else decode(p, w, u);
+}
+
+// Live key runs of query row i under the frame-blind tiling (the padded tail
+// takes the last frame's): [lo0, hi0) and [lo1, hi1), possibly empty.
+__device__ __forceinline__ void row_runs(const Params &p, int i, int &lo0, int &hi0, int &lo1, int &hi1) {
+    const int f = min(i, p.N - 1) / p.T;
+    const int wlo = max(0, f - p.W), whi = min(p.F - 1, f + p.W);
+    const bool ref_out = p.ref >= 0 && (p.ref < wlo || p.ref > whi);
+    lo0 = hi0 = lo1 = hi1 = 0;
+    if (p.part != VDIT_PART_REFERENCE) { lo0 = wlo * p.T; hi0 = (whi + 1) * p.T; }
+    if (p.part != VDIT_PART_WINDOW && ref_out) { lo1 = p.ref * p.T; hi1 = (p.ref + 1) * p.T; }
 }
 
 // first row of query tile q of the unit (last tile of a segment ends at its end)
@@ -220,7 +287,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-template <int D>
+template <int D, bool kTiled>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -281,7 +348,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x) {
                 Work u;
-                decode(p, w, u);
+                decode_any<kTiled>(p, w, u);
+                if (kTiled && u.nkt == 0) continue;   // a block with no live key: no work
                 if (!(ok = mbar_wait(bar(kBarQfree), (it & 1) ^ 1, abort_flag, p.status, kSiteQfree, tlim)))
                     break;
                 mbar_arrive_expect_tx(bar(kBarQfull), (uint32_t)(u.nact * L::kTileBytes));
@@ -370,7 +438,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
-            decode(p, w, u);
+            decode_any<kTiled>(p, w, u);
+            if (kTiled && u.nkt == 0) { --it; continue; }   // skipped by every role: no phase used
             if (!(ok = wait(kBarQfull, it & 1, kSiteQfullMma))) break;
             const uint32_t kc0 = kc;
             int start, nvalid;
@@ -490,7 +559,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
-            decode(p, w, u);
+            decode_any<kTiled>(p, w, u);
+            if (kTiled && u.nkt == 0) {
+                // skipped by every role (no phase used): a block none of whose rows
+                // sees a key of this part of the mask stores O = 0 and LSE = -inf
+                const int row = tile_row(u, q) + r;
+                if (q < u.nact && row < p.N) {
+                    const long long obase = (long long)u.b * p.os0 + (long long)u.h * p.os1 + (long long)row * p.os2;
+                    for (int c0 = 0; c0 < D; c0 += 8) {
+                        if (p.o_f32) {
+                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + obase + c0);
+                            dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + obase + c0) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    if (p.lse) p.lse[((long long)u.bh * p.N) + row] = -INFINITY;
+                }
+                --it;
+                continue;
+            }
             const bool act = q < u.nact || u.alt;
             // The last active warpgroup releases K, V and Q tiles: its S barrier for key
             // tile j is committed after every earlier MMA of the unit (all S MMAs of
@@ -537,7 +627,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!act) continue;
 
             float l0 = 0.f, l1 = 0.f, mrun = -INFINITY;
-            for (int j = u.alt ? q : 0; j < u.nkt; j += u.alt ? 2 : 1) {
+            const int j0 = u.alt ? q : 0;          // this warpgroup's first key tile
+            int rlo0 = 0, rhi0 = 0, rlo1 = 0, rhi1 = 0;   // frame-blind tiling: this row's live keys
+            if constexpr (kTiled) row_runs(p, tile_row(u, u.alt ? 0 : q) + r, rlo0, rhi0, rlo1, rhi1);
+            for (int j = j0; j < u.nkt; j += u.alt ? 2 : 1) {
                 int start, nvalid;
                 key_tile(u, j, start, nvalid);
                 ok = mbar_wait_warp(bar(kBarSfull + q), sq & 1, abort_flag, p.status, kSiteSfull, tlim);
@@ -555,46 +648,64 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (j >= 2) mbar_arrive(bar(kBarVfree + (kc0 + j - 2) % kStagesV));
                     if (j == u.nkt - 1) mbar_arrive(bar(kBarQfree));
                 }
-                float mrow = mt;
-                if (!stat) {
-                    // online: this tile's row max (pass 1), lazy rescale of O
-                    float mx = -INFINITY;
-                    {
-                        uint32_t v[128];
-                        tmem_ld128(tS, v);
+                // the whole 128-column S row in one TMEM load
+                uint32_t v[128];
+                tmem_ld128(tS, v);
+                if constexpr (kTiled) {
+                    // a tile that straddles a frame boundary: the mask predicate, per
+                    // element, turns this row's dead keys (and padding) into -inf
+                    const bool full = (rlo0 <= start && start + kBK <= rhi0) ||
+                                      (rlo1 <= start && start + kBK <= rhi1);
+                    if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
                         for (int e = 0; e < 128; ++e) {
-                            const float x = __uint_as_float(v[e]) * sc;
-                            mx = (e < nvalid) ? fmaxf(mx, x) : mx;
+                            const int jk = start + e;
+                            const bool live = (unsigned)(jk - rlo0) < (unsigned)(rhi0 - rlo0) ||
+                                              (unsigned)(jk - rlo1) < (unsigned)(rhi1 - rlo1);
+                            v[e] = live ? v[e] : 0xff800000u;
                         }
                     }
-                    if (j == 0) {
+                }
+                float mrow = mt;
+                float alpha = 1.f;      // online: factor of the O rescale (lazy, warp-uniform)
+                bool rescale = false;
+                if (!stat) {
+                    // online: this tile's row max, taken on the raw logits (the scale
+                    // is positive), then the lazy rescale decision
+                    float mx;
+                    if (nvalid >= kBK) {
+                        float m8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(v[e]);
+#pragma unroll
+                        for (int e = 8; e < 128; ++e) m8[e % 8] = fmaxf(m8[e % 8], __uint_as_float(v[e]));
+                        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    } else {
+                        mx = -INFINITY;
+#pragma unroll
+                        for (int e = 0; e < 128; ++e) mx = e < nvalid ? fmaxf(mx, __uint_as_float(v[e])) : mx;
+                    }
+                    mx *= sc;
+                    if (j == j0) {
                         mrun = mx;
                     } else {
                         const bool need = mx > mrun + kLazyRescale;
                         if (__any_sync(0xffffffffu, need)) {
-                            const float alpha = need ? ex2(mrun - mx) : 1.f;
-#pragma unroll
-                            for (int c0 = 0; c0 < D; c0 += 32) {
-                                uint32_t v[32];
-                                tmem_ld32(tO + c0, v);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                                tmem_st32(tO + c0, v);
-                            }
+                            rescale = true;
+                            alpha = need ? ex2(mrun - mx) : 1.f;
                             l0 *= alpha;
                             l1 *= alpha;
                             if (need) mrun = mx;
                         }
                     }
                     mrow = mrun;
+                    // no live key in this row yet (frame-blind tiling): every term is
+                    // masked, any finite shift gives p = 0
+                    if constexpr (kTiled) mrow = mrow == -INFINITY ? 0.f : mrow;
                 }
-                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S;
-                // the whole 128-column S row in one TMEM load
+                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S
                 {
-                    uint32_t v[128];
-                    tmem_ld128(tS, v);
                     const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-mrow, -mrow);
                     uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -609,8 +720,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                 float x0, x1;
                                 f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i0]), __uint_as_float(v[i0 + 1])), sc2, nm2),
                                           x0, x1);
-                                const float p0 = softmax_exp2<2 * e>(x0);
-                                const float p1 = softmax_exp2<2 * e + 1>(x1);
+                                const float p0 = ex2(x0);
+                                const float p1 = ex2(x1);
                                 l2 = f2_add(l2, f2_pack(p0, p1));
                                 pk[e] = pack_bf16(p0, p1);
                             });
@@ -633,6 +744,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     l0 += a0;
                     l1 += a1;
                 }
+                if (rescale) {
+                    // O (after P.V of the previous key tile, which the S barrier of this
+                    // tile covers) scaled to the new running max, before this tile's P.V
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c0, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + c0, o);
+                    }
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -642,12 +765,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             if (!ok) break;
             float l = l0 + l1;
+            float w0 = 1.f, w1 = 1.f;   // weights of O0 and O1 in an alternating online unit
             if (u.alt) {
-                // warpgroup 1 hands its row sums to warpgroup 0, which writes the tile
+                // warpgroup 1 hands its row sums (and, online, its running max) to
+                // warpgroup 0, which writes the tile
                 if (q == 1) {
                     ok = mbar_wait_warp(bar(kBarXfree), (xc & 1) ^ 1, abort_flag, p.status, kSiteXfree, tlim);
                     if (!ok) break;
                     xbuf[r] = l;
+                    xbuf[kTileRows + r] = mt;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kBarXfull));
                     ++xc;
@@ -656,7 +782,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 ok = mbar_wait_warp(bar(kBarXfull), xc & 1, abort_flag, p.status, kSiteXfull, tlim);
                 if (!ok) break;
-                l += xbuf[r];
+                if (stat) {
+                    l += xbuf[r];       // both halves share the static bound
+                } else {
+                    // online halves have their own running maxima m0, m1: rescale both
+                    // to M = max(m0, m1), which is exact (softmax is shift-invariant)
+                    const float m1 = xbuf[kTileRows + r], M = fmaxf(mt, m1);
+                    w0 = ex2(mt - M);
+                    w1 = ex2(m1 - M);
+                    if constexpr (kTiled) {
+                        // a half that saw no live key has l = 0 and takes no weight
+                        w0 = mt == -INFINITY ? 0.f : w0;
+                        w1 = m1 == -INFINITY ? 0.f : w1;
+                    }
+                    l = l * w0 + xbuf[r] * w1;
+                    mt = M;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarXfree));
                 ++xc;
@@ -672,13 +813,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(bar(kBarVfree + (kc0 + u.nkt - 1) % kStagesV));
             }
             // epilogue: O / l for the rows this tile owns, and LSE (alternating
-            // units: O = O0 + O1)
-            const float inv = 1.0f / l;
+            // units: O = O0 + O1, online O = w0 O0 + w1 O1)
+            // a row that saw no live key at all (possible only for a part of the
+            // mask under the frame-blind tiling) stores O = 0 and LSE = -inf
+            const float inv = kTiled && l == 0.f ? 0.f : 1.0f / l;
             const int t = kTilesPerUnit * u.pair + q;
             const int row = tile_row(u, q) + r;
             const int own_lo = u.row0 + t * kTileRows;
             const int own_hi = u.row0 + min((t + 1) * kTileRows, u.rows);
-            const bool owned = row >= own_lo && row < own_hi;
+            const bool owned = row >= own_lo && row < own_hi && (!kTiled || row < p.N);
             const long long obase = (long long)u.b * p.os0 + (long long)u.h * p.os1 + (long long)row * p.os2;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -687,9 +830,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (u.alt) {
                     uint32_t v1[32];
                     tmem_ld32(tO1 + c0, v1);
+                    if (stat) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v1[e]));
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v1[e]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(fmaf(__uint_as_float(v[e]), w0, __uint_as_float(v1[e]) * w1));
+                    }
                 }
                 if (owned) {
                     if (p.o_f32) {
@@ -777,16 +926,64 @@ static_assert(Layout<64>::kBytes <= Layout<64>::kAlloc && Layout<64>::kAlloc <= 
               "the D = 64 layout must fit the shared-memory request");
 static_assert(kSmemRequest <= 227 * 1024, "shared memory beyond the per-CTA limit");
 
-template <int D>
+template <int D, bool kTiled>
 cudaError_t prepare_kernel(int device) {
     static std::mutex mu;
     static bool done[64] = {};
     std::lock_guard<std::mutex> g(mu);
     if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kTiled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemRequest);
     if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
     return e;
+}
+
+// Merge of two partial attention results over disjoint key sets (the window
+// pass a and the reference pass b of the two-pass form): per row, with
+// M = max(LSE_a, LSE_b), w_x = exp(LSE_x - M),
+//   O = (w_a O_a + w_b O_b) / (w_a + w_b),   LSE = M + ln(w_a + w_b).
+// Rows whose frame has no key in plan b take pass a unchanged. One warp per
+// row; O_a, O_b fp32 [BH, N, D] and LSE_a, LSE_b fp32 [BH, N], dense.
+__global__ void merge_kernel(const float *oa, const float *la, const float *ob, const float *lb,
+                             const int32_t *runs_b, int T, int N, int H, long long rows, int D,
+                             void *o, long long os0, long long os1, long long os2, int o_f32,
+                             float *lse) {
+    const int lane = threadIdx.x % 32;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long rw = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; rw < rows; rw += nwarps) {
+        const int bh = (int)(rw / N), i = (int)(rw % N), f = i / T;
+        const int32_t *rb = runs_b + 4 * f;
+        const bool has_b = rb[1] > rb[0] || rb[3] > rb[2];
+        const float lsa = la[rw];
+        float wa = 1.f, wb = 0.f, L = lsa;
+        if (has_b) {
+            const float lsb = lb[rw], M = fmaxf(lsa, lsb);
+            wa = expf(lsa - M);
+            wb = expf(lsb - M);
+            const float sum = wa + wb;
+            wa /= sum;
+            wb /= sum;
+            L = M + logf(sum);
+        }
+        const long long obase = (long long)(bh / H) * os0 + (long long)(bh % H) * os1 + (long long)i * os2;
+        for (int c = lane * 4; c < D; c += 128) {
+            const float4 a = *reinterpret_cast<const float4 *>(oa + rw * D + c);
+            float4 r = make_float4(a.x * wa, a.y * wa, a.z * wa, a.w * wa);
+            if (has_b) {
+                const float4 b = *reinterpret_cast<const float4 *>(ob + rw * D + c);
+                r = make_float4(fmaf(b.x, wb, r.x), fmaf(b.y, wb, r.y), fmaf(b.z, wb, r.z), fmaf(b.w, wb, r.w));
+            }
+            if (o_f32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(o) + obase + c) = r;
+            } else {
+                uint2 pk;
+                pk.x = pack_bf16(r.x, r.y);
+                pk.y = pack_bf16(r.z, r.w);
+                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(o) + obase + c) = pk;
+            }
+        }
+        if (lse && lane == 0) lse[rw] = L;
+    }
 }
 
 int sm_count(int device) {
@@ -814,7 +1011,7 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
                           const int64_t v_strides[3], const int64_t o_strides[3], float scale,
                           const float *k_mean, const float *k_rmax, const uint8_t *eligible,
                           const float *seg_rmax, const uint8_t *seg_elig, int32_t mode,
-                          void *stream) {
+                          void *stream, bool tiled = false) {
     clear_error();
     if (!plan) { set_error("vdit_attn_fwd: plan is NULL"); return VDIT_ERR_INVALID; }
     if (!q || !k || !v || !o || !q_strides || !k_strides || !v_strides || !o_strides) {
@@ -890,20 +1087,39 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
     prm.mode = mode;
     prm.status = plan->d_status;
     prm.timeout_ns = wait_limit_ns();
+    prm.F = plan->F; prm.T = plan->T; prm.W = plan->W; prm.ref = plan->ref; prm.part = plan->part;
+    prm.n_blocks = (int)((N + kTilesPerUnit * kTileRows - 1) / (kTilesPerUnit * kTileRows));
+    if (tiled) prm.total_work = (long long)B * H * prm.n_blocks;
     const int nsm = sm_count(dev);
     if (nsm <= 0) { set_error("vdit_attn_fwd: cannot query SM count"); return VDIT_ERR_CUDA; }
     const long long grid = prm.total_work < nsm ? prm.total_work : nsm;
     if (grid <= 0) return VDIT_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (D == 128) {
-        VDIT_CUDA_TRY(prepare_kernel<128>(dev));
-        attn_fwd_kernel<128><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    if (launch_fails_by_hook()) {
+        set_error("vdit_attn_fwd: launch failure injected by vdit_set_launch_fail_after");
+        return VDIT_ERR_CUDA;
+    }
+    if (D == 128 && !tiled) {
+        VDIT_CUDA_TRY((prepare_kernel<128, false>(dev)));
+        attn_fwd_kernel<128, false><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    } else if (D == 64 && !tiled) {
+        VDIT_CUDA_TRY((prepare_kernel<64, false>(dev)));
+        attn_fwd_kernel<64, false><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    } else if (D == 128) {
+        VDIT_CUDA_TRY((prepare_kernel<128, true>(dev)));
+        attn_fwd_kernel<128, true><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
     } else {
-        VDIT_CUDA_TRY(prepare_kernel<64>(dev));
-        attn_fwd_kernel<64><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+        VDIT_CUDA_TRY((prepare_kernel<64, true>(dev)));
+        attn_fwd_kernel<64, true><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
     }
     VDIT_CUDA_TRY(cudaGetLastError());
     return VDIT_OK;
+}
+
+size_t two_pass_bytes(int32_t B, int32_t H, long long N, int32_t D) {
+    const size_t rows = (size_t)B * H * (size_t)N;
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    return 2 * (al(rows * D * 4) + al(rows * 4));
 }
 
 }  // namespace
@@ -942,4 +1158,87 @@ extern "C" vdit_status vdit_attn_fwd_framed(const vdit_plan *plan, const void *q
     return attn_fwd_impl(plan, q, k, v, o, o_dtype, lse, B, H, D, q_strides, k_strides, v_strides,
                          o_strides, scale, k_mean, seg_rmax, seg_eligible, seg_rmax, seg_eligible,
                          mode, stream);
+}
+
+extern "C" vdit_status vdit_attn_fwd_tiles128(const vdit_plan *plan, const void *q, const void *k,
+                                              const void *v, void *o, int32_t o_dtype, float *lse,
+                                              int32_t B, int32_t H, int32_t D, const int64_t q_strides[3],
+                                              const int64_t k_strides[3], const int64_t v_strides[3],
+                                              const int64_t o_strides[3], float scale, const float *k_mean,
+                                              const float *k_rmax, const uint8_t *eligible, int32_t mode,
+                                              void *stream) {
+    return attn_fwd_impl(plan, q, k, v, o, o_dtype, lse, B, H, D, q_strides, k_strides, v_strides,
+                         o_strides, scale, k_mean, k_rmax, eligible, nullptr, nullptr, mode, stream, true);
+}
+
+extern "C" size_t vdit_attn_two_pass_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D) {
+    if (B < 1 || H < 1 || N < 1 || D < 1) return 0;
+    return two_pass_bytes(B, H, N, D);
+}
+
+extern "C" vdit_status vdit_attn_fwd_two_pass(const vdit_plan *plan_window, const vdit_plan *plan_reference,
+                                              const void *q, const void *k, const void *v, void *o,
+                                              int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
+                                              const int64_t q_strides[3], const int64_t k_strides[3],
+                                              const int64_t v_strides[3], const int64_t o_strides[3],
+                                              float scale, const float *k_mean, const float *k_rmax,
+                                              const uint8_t *eligible, int32_t mode, int32_t tiles,
+                                              void *workspace, size_t workspace_bytes, void *stream) {
+    clear_error();
+    if (!plan_window || !plan_reference) {
+        set_error("vdit_attn_fwd_two_pass: plan is NULL");
+        return VDIT_ERR_INVALID;
+    }
+    const vdit_plan *a = plan_window, *b = plan_reference;
+    if (a->part != VDIT_PART_WINDOW || b->part != VDIT_PART_REFERENCE || a->F != b->F || a->T != b->T ||
+        a->W != b->W || a->ref != b->ref || a->device != b->device) {
+        set_error("vdit_attn_fwd_two_pass: needs the window part and the reference part of one mask");
+        return VDIT_ERR_INVALID;
+    }
+    if (tiles != VDIT_TILES_FRAME && tiles != VDIT_TILES_128) {
+        set_error("vdit_attn_fwd_two_pass: tiles=%d invalid", tiles);
+        return VDIT_ERR_INVALID;
+    }
+    if (!o || !o_strides || (o_dtype != VDIT_O_BF16 && o_dtype != VDIT_O_F32) || B < 1 || H < 1 ||
+        (D != 64 && D != 128)) {
+        set_error("vdit_attn_fwd_two_pass: invalid output, sizes or o_dtype");
+        return D == 64 || D == 128 ? VDIT_ERR_INVALID : VDIT_ERR_UNSUPPORTED;
+    }
+    const int oal = o_dtype == VDIT_O_F32 ? 4 : 8;
+    for (int i = 0; i < 3; ++i)
+        if (o_strides[i] <= 0 || o_strides[i] % oal != 0) {
+            set_error("vdit_attn_fwd_two_pass: o strides must be positive multiples of 16 bytes");
+            return VDIT_ERR_INVALID;
+        }
+    if (!aligned16(o)) { set_error("vdit_attn_fwd_two_pass: o must be 16-byte aligned"); return VDIT_ERR_INVALID; }
+    const long long N = a->N;
+    const size_t need = two_pass_bytes(B, H, N, D);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
+        set_error("vdit_attn_fwd_two_pass: workspace needs %zu bytes, 256-byte aligned (got %zu)", need,
+                  workspace_bytes);
+        return VDIT_ERR_INVALID;
+    }
+    const size_t rows = (size_t)B * H * (size_t)N;
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    float *oa = reinterpret_cast<float *>(w);
+    float *la = reinterpret_cast<float *>(w + al(rows * D * 4));
+    float *ob = reinterpret_cast<float *>(w + al(rows * D * 4) + al(rows * 4));
+    float *lb = reinterpret_cast<float *>(w + 2 * al(rows * D * 4) + al(rows * 4));
+    const int64_t dst[3] = {(int64_t)H * N * D, (int64_t)N * D, (int64_t)D};
+    const bool tiled = tiles == VDIT_TILES_128;
+    vdit_status st = attn_fwd_impl(a, q, k, v, oa, VDIT_O_F32, la, B, H, D, q_strides, k_strides, v_strides,
+                                   dst, scale, k_mean, k_rmax, eligible, nullptr, nullptr, mode, stream, tiled);
+    if (st != VDIT_OK) return st;
+    st = attn_fwd_impl(b, q, k, v, ob, VDIT_O_F32, lb, B, H, D, q_strides, k_strides, v_strides, dst, scale,
+                       k_mean, k_rmax, eligible, nullptr, nullptr, mode, stream, tiled);
+    if (st != VDIT_OK) return st;
+    const int nsm = sm_count(a->device);
+    const long long blocks = ((long long)rows + 7) / 8;   // 8 warps (rows) per block
+    const long long grid = blocks < 16LL * nsm ? blocks : 16LL * nsm;
+    merge_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        oa, la, ob, lb, b->d_frame_runs, b->T, (int)N, H, (long long)rows, D, o, o_strides[0], o_strides[1],
+        o_strides[2], o_dtype == VDIT_O_F32, lse);
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
 }

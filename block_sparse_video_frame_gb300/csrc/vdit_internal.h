@@ -33,6 +33,10 @@ unsigned long long wait_limit_ns();
 // every device allocation the library makes goes through here.
 cudaError_t device_alloc(void **ptr, size_t bytes);
 
+// Launch-failure test hook (vdit_set_launch_fail_after): true for the one
+// attention launch that is to fail as if the launch had been refused.
+bool launch_fails_by_hook();
+
 // Query-tile geometry shared by the plan and the attention kernel.
 constexpr int kTileRows = 128;   // rows of one query tile (tcgen05 M)
 constexpr int kTilesPerUnit = 2; // query tiles that share one K/V stream
@@ -58,6 +62,7 @@ struct PlanHeader {
 
 struct vdit_plan {
     int F, T, W, ref, bs, dense;
+    int part = VDIT_PART_ALL;   // which part of the mask the plan schedules
     long long N;
     int n_qblocks;
     vdit::PlanHeader h;  // host copy of the header

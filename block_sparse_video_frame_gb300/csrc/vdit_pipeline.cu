@@ -96,6 +96,7 @@ struct vdit_pipeline {
     Slot slot[kSlots];
     cudaStream_t s_in = nullptr, s_out = nullptr, s_cmp[kSlots] = {};
     cudaEvent_t start = nullptr;
+    cudaEvent_t join[2 + kSlots] = {};   // error path: the caller's stream waits for every internal stream
 };
 
 namespace {
@@ -109,6 +110,8 @@ void release(vdit_pipeline *p) {
         if (s.out_done) cudaEventDestroy(s.out_done);
     }
     if (p->start) cudaEventDestroy(p->start);
+    for (cudaEvent_t e : p->join)
+        if (e) cudaEventDestroy(e);
     if (p->s_in) cudaStreamDestroy(p->s_in);
     for (cudaStream_t s : p->s_cmp)
         if (s) cudaStreamDestroy(s);
@@ -285,7 +288,9 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
             }
         }
     }
-    if ((e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming)) == cudaSuccess &&
+    for (cudaEvent_t &j : p->join)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming);
+    if (e == cudaSuccess && (e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming)) == cudaSuccess &&
         (e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking)) == cudaSuccess)
         e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking);
     for (int i = 0; i < kSlots && e == cudaSuccess; ++i)
@@ -298,45 +303,25 @@ extern "C" vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, in
     return VDIT_OK;
 }
 
-extern "C" vdit_status vdit_pipeline_run(vdit_pipeline *p, const void *q_host, const void *k_host,
-                                         const void *v_host, void *o_host, float *lse_host,
-                                         const int64_t host_strides[3], float scale, float tau,
-                                         int32_t mode, void *stream) {
-    clear_error();
-    if (!p) { set_error("vdit_pipeline_run: pipeline is NULL"); return VDIT_ERR_INVALID; }
-    if (!q_host || !k_host || !v_host || !o_host || !host_strides) {
-        set_error("vdit_pipeline_run: NULL pointer argument");
-        return VDIT_ERR_INVALID;
-    }
-    for (int i = 0; i < 3; ++i)
-        if (host_strides[i] <= 0) {
-            set_error("vdit_pipeline_run: host strides must be positive");
-            return VDIT_ERR_INVALID;
-        }
-    if (host_strides[2] < p->D) {
-        set_error("vdit_pipeline_run: host token stride is below D");
-        return VDIT_ERR_INVALID;
-    }
-    // checked here too, before any copy is queued (the per-group calls repeat them)
-    if (!finite_positive(scale) || !(tau >= 0.f)) {
-        set_error("vdit_pipeline_run: scale must be finite and > 0, tau >= 0");
-        return VDIT_ERR_INVALID;
-    }
-    if (mode < VDIT_MODE_AUTO || mode > VDIT_MODE_FORCE_STATIC) {
-        set_error("vdit_pipeline_run: mode=%d invalid", mode);
-        return VDIT_ERR_INVALID;
-    }
-    int dev = -1;
-    VDIT_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev != p->device) {
-        set_error("vdit_pipeline_run: pipeline was created on device %d, current device is %d", p->device, dev);
-        return VDIT_ERR_INVALID;
-    }
-    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+namespace {
+
+// Queues every head group of one run (see vdit_pipeline_run). Returns at the
+// first error; what was queued before it stays queued.
+vdit_status enqueue_groups(vdit_pipeline *p, const void *q_host, const void *k_host, const void *v_host,
+                           void *o_host, float *lse_host, const int64_t host_strides[3], float scale,
+                           float tau, int32_t mode, cudaStream_t caller) {
     VDIT_CUDA_TRY(cudaEventRecord(p->start, caller));
     VDIT_CUDA_TRY(cudaStreamWaitEvent(p->s_in, p->start, 0));
     for (cudaStream_t sc : p->s_cmp) VDIT_CUDA_TRY(cudaStreamWaitEvent(sc, p->start, 0));
     VDIT_CUDA_TRY(cudaStreamWaitEvent(p->s_out, p->start, 0));
+    // A previous run may have been queued on another stream: the first groups of
+    // this run reuse its slots only after its kernels and copies of those slots
+    // are done (on one stream the start event already orders this; an event never
+    // recorded is a wait that completes at once).
+    for (int i = 0; i < kSlots; ++i) {
+        VDIT_CUDA_TRY(cudaStreamWaitEvent(p->s_in, p->slot[i].computed, 0));
+        VDIT_CUDA_TRY(cudaStreamWaitEvent(p->s_cmp[i], p->slot[i].out_done, 0));
+    }
     const int B = p->B, N = p->N, D = p->D, H = p->H;
     for (int g = 0; g < p->groups; ++g) {
         const int h0 = p->first[g], hc = p->first[g + 1] - h0;
@@ -384,6 +369,57 @@ extern "C" vdit_status vdit_pipeline_run(vdit_pipeline *p, const void *q_host, c
     for (int i = 0; i < kSlots && i < p->groups; ++i)
         VDIT_CUDA_TRY(cudaStreamWaitEvent(caller, p->slot[i].out_done, 0));
     return VDIT_OK;
+}
+
+}  // namespace
+
+extern "C" vdit_status vdit_pipeline_run(vdit_pipeline *p, const void *q_host, const void *k_host,
+                                         const void *v_host, void *o_host, float *lse_host,
+                                         const int64_t host_strides[3], float scale, float tau,
+                                         int32_t mode, void *stream) {
+    clear_error();
+    if (!p) { set_error("vdit_pipeline_run: pipeline is NULL"); return VDIT_ERR_INVALID; }
+    if (!q_host || !k_host || !v_host || !o_host || !host_strides) {
+        set_error("vdit_pipeline_run: NULL pointer argument");
+        return VDIT_ERR_INVALID;
+    }
+    for (int i = 0; i < 3; ++i)
+        if (host_strides[i] <= 0) {
+            set_error("vdit_pipeline_run: host strides must be positive");
+            return VDIT_ERR_INVALID;
+        }
+    if (host_strides[2] < p->D) {
+        set_error("vdit_pipeline_run: host token stride is below D");
+        return VDIT_ERR_INVALID;
+    }
+    // checked here too, before any copy is queued (the per-group calls repeat them)
+    if (!finite_positive(scale) || !(tau >= 0.f)) {
+        set_error("vdit_pipeline_run: scale must be finite and > 0, tau >= 0");
+        return VDIT_ERR_INVALID;
+    }
+    if (mode < VDIT_MODE_AUTO || mode > VDIT_MODE_FORCE_STATIC) {
+        set_error("vdit_pipeline_run: mode=%d invalid", mode);
+        return VDIT_ERR_INVALID;
+    }
+    int dev = -1;
+    VDIT_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev != p->device) {
+        set_error("vdit_pipeline_run: pipeline was created on device %d, current device is %d", p->device, dev);
+        return VDIT_ERR_INVALID;
+    }
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    const vdit_status st = enqueue_groups(p, q_host, k_host, v_host, o_host, lse_host, host_strides, scale,
+                                          tau, mode, caller);
+    if (st != VDIT_OK) {
+        // Copies and kernels of earlier groups may still be queued on the internal
+        // streams: the caller's stream waits for all of them, so that synchronising
+        // it still covers every access to the host buffers.
+        cudaStream_t ss[2 + kSlots] = {p->s_in, p->s_out};
+        for (int i = 0; i < kSlots; ++i) ss[2 + i] = p->s_cmp[i];
+        for (int i = 0; i < 2 + kSlots; ++i)
+            if (cudaEventRecord(p->join[i], ss[i]) == cudaSuccess) cudaStreamWaitEvent(caller, p->join[i], 0);
+    }
+    return st;
 }
 
 extern "C" void vdit_pipeline_destroy(vdit_pipeline *p) {

@@ -25,7 +25,7 @@ namespace vdit {
 namespace {
 
 struct PlanArgs {
-    int F, T, W, ref, bs, dense;
+    int F, T, W, ref, bs, dense, part;
     long long N;
     int nqb;
     int units_cap;
@@ -38,14 +38,24 @@ __device__ __forceinline__ void frame_window(const PlanArgs &a, int f, int &wlo,
 }
 
 // Live key frames of frame f, as at most two maximal token runs [lo, hi).
+// Part 1 keeps the window alone, part 2 the reference frame alone (for frames
+// whose window does not contain it; other frames see no key).
 __device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_frames) {
     int wlo, whi;
     frame_window(a, f, wlo, whi);
     long long T = a.T;
+    const int g = a.ref;
+    const bool ref_outside = g >= 0 && (g < wlo || g > whi);
+    if (a.part == VDIT_PART_REFERENCE) {
+        live_frames = ref_outside ? 1 : 0;
+        r[0] = ref_outside ? (int)(g * T) : 0;
+        r[1] = ref_outside ? (int)((g + 1) * T) : 0;
+        r[2] = 0; r[3] = 0;
+        return;
+    }
     live_frames = whi - wlo + 1;
     int lo0 = (int)(wlo * T), hi0 = (int)((whi + 1) * T), lo1 = 0, hi1 = 0;
-    const int g = a.ref;
-    if (g >= 0 && (g < wlo || g > whi)) {
+    if (ref_outside && a.part == VDIT_PART_ALL) {
         live_frames += 1;
         if (g == wlo - 1) {
             lo0 = (int)(g * T);                       // adjacent below: merge
@@ -130,6 +140,7 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_run
     for (int i = 0; i < nseg; ++i) {
         int s = s_order[i];
         const int32_t *g = segments + kSegInts * s;
+        if (g[7] == 0) break;   // frames that see no key (reference part only): no work, sorted last
         if (g[7] != prev_key) {
             if (ncls >= kMaxClasses) { h.error = 2; break; }
             class_off[ncls++] = nu;
@@ -182,9 +193,47 @@ __global__ void plan_csr_kernel(PlanArgs a, const int32_t *frame_runs, int32_t *
     }
 }
 
+// Census of the tile x tile grid over the N x N token pairs (the last tile of
+// each axis ragged when tile does not divide N): a tile is full when every
+// token pair in it is live, dead when none is, partial otherwise. The mask
+// depends only on the frames of the two tokens, so a tile is classified from
+// the frame pairs it covers. One thread per tile, block-wide sums, three
+// atomics per block.
+__global__ void census_kernel(int F, int T, int W, int ref, long long N, int tile, long long nb,
+                              unsigned long long *counts) {
+    __shared__ unsigned long long s_cnt[3];
+    if (threadIdx.x < 3) s_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    unsigned long long c[3] = {0, 0, 0};
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < nb * nb;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long qb = t / nb, kb = t % nb;
+        const long long i0 = qb * tile, i1 = min(i0 + tile, N);
+        const long long j0 = kb * tile, j1 = min(j0 + tile, N);
+        const int fa = (int)(i0 / T), fb = (int)((i1 - 1) / T);
+        const int ga = (int)(j0 / T), gb = (int)((j1 - 1) / T);
+        bool all = true, any = false;
+        for (int f = fa; f <= fb; ++f)
+            for (int g = ga; g <= gb; ++g) {
+                const int d = f > g ? f - g : g - f;
+                const bool live = d <= W || g == ref;
+                all = all && live;
+                any = any || live;
+            }
+        c[all ? 0 : (any ? 1 : 2)] += 1;
+    }
+    for (int i = 0; i < 3; ++i) {
+        unsigned long long v = c[i];
+        for (int o = 16; o > 0; o /= 2) v += __shfl_down_sync(0xffffffffu, v, o);
+        if ((threadIdx.x & 31) == 0 && v) atomicAdd(&s_cnt[i], v);
+    }
+    __syncthreads();
+    if (threadIdx.x < 3 && s_cnt[threadIdx.x]) atomicAdd(&counts[threadIdx.x], s_cnt[threadIdx.x]);
+}
+
 PlanArgs args_of(const vdit_plan *p) {
     PlanArgs a;
-    a.F = p->F; a.T = p->T; a.W = p->W; a.ref = p->ref; a.bs = p->bs; a.dense = p->dense;
+    a.F = p->F; a.T = p->T; a.W = p->W; a.ref = p->ref; a.bs = p->bs; a.dense = p->dense; a.part = p->part;
     a.N = p->N; a.nqb = p->n_qblocks; a.units_cap = p->units_cap;
     return a;
 }
@@ -217,8 +266,10 @@ cudaError_t launch_plan_kernels(const vdit_plan *p, cudaStream_t stream, bool cs
 
 using namespace vdit;
 
-extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs,
-                                      void *stream, vdit_plan **out) {
+namespace {
+
+vdit_status plan_create(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs, int32_t part,
+                        void *stream, vdit_plan **out) {
     clear_error();
     if (!out) { set_error("vdit_attn_plan: out is NULL"); return VDIT_ERR_INVALID; }
     *out = nullptr;
@@ -241,6 +292,15 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
         return VDIT_ERR_INVALID;
     }
     const int dense = W >= F - 1 ? 1 : 0;
+    if (part != VDIT_PART_ALL && part != VDIT_PART_WINDOW && part != VDIT_PART_REFERENCE) {
+        set_error("vdit_attn_plan_part: part=%d invalid", part);
+        return VDIT_ERR_INVALID;
+    }
+    if (part != VDIT_PART_ALL && (dense || ref < 0)) {
+        set_error("vdit_attn_plan_part: the mask has no separate reference part (%s)",
+                  dense ? "the window covers every frame" : "no reference frame");
+        return VDIT_ERR_INVALID;
+    }
     if (!dense && T % bs != 0) {
         set_error("vdit_attn_plan: block_size=%d does not divide tokens_per_frame=%d "
                   "(blocks would straddle frame boundaries)", bs, T);
@@ -249,7 +309,7 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     vdit_plan *p = new (std::nothrow) vdit_plan();
     if (!p) { set_error("vdit_attn_plan: host allocation failed"); return VDIT_ERR_NOMEM; }
-    p->F = F; p->T = T; p->W = W; p->ref = ref; p->bs = bs; p->dense = dense;
+    p->F = F; p->T = T; p->W = W; p->ref = ref; p->bs = bs; p->dense = dense; p->part = part;
     p->N = (long long)F * T;
     p->n_qblocks = (int)((p->N + bs - 1) / bs);
     p->units_cap = (int)(p->N / (kTileRows * kTilesPerUnit)) + 2 * F + 2;
@@ -309,6 +369,18 @@ extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t r
     return VDIT_OK;
 }
 
+}  // namespace
+
+extern "C" vdit_status vdit_attn_plan(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs,
+                                      void *stream, vdit_plan **out) {
+    return plan_create(F, T, W, ref, bs, VDIT_PART_ALL, stream, out);
+}
+
+extern "C" vdit_status vdit_attn_plan_part(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs,
+                                           int32_t part, void *stream, vdit_plan **out) {
+    return plan_create(F, T, W, ref, bs, part, stream, out);
+}
+
 extern "C" vdit_status vdit_plan_rebuild(vdit_plan *p, void *stream) {
     clear_error();
     if (!p) { set_error("vdit_plan_rebuild: plan is NULL"); return VDIT_ERR_INVALID; }
@@ -333,6 +405,7 @@ extern "C" vdit_status vdit_plan_get_info(const vdit_plan *p, vdit_plan_info *in
     info->n_segments = p->h.n_segments;
     info->n_units = p->h.n_units;
     info->n_classes = p->h.n_classes;
+    info->part = p->part;
     info->d_row_ptr = p->d_row_ptr;
     info->d_col_idx = p->d_col_idx;
     info->d_frame_runs = p->d_frame_runs;
@@ -368,4 +441,28 @@ extern "C" void vdit_plan_destroy(vdit_plan *p) {
     free_plan_buffers(p);
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     delete p;
+}
+
+extern "C" vdit_status vdit_plan_block_census(const vdit_plan *p, int32_t tile, int64_t *counts,
+                                              void *stream) {
+    clear_error();
+    if (!p || !counts) { set_error("vdit_plan_block_census: NULL argument"); return VDIT_ERR_INVALID; }
+    if (tile < 16 || tile % 16 != 0) {
+        set_error("vdit_plan_block_census: tile=%d is not a positive multiple of 16", tile);
+        return VDIT_ERR_INVALID;
+    }
+    if ((reinterpret_cast<uintptr_t>(counts) & 7u) != 0) {
+        set_error("vdit_plan_block_census: counts must be 8-byte aligned");
+        return VDIT_ERR_INVALID;
+    }
+    const long long nb = (p->N + tile - 1) / tile;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    VDIT_CUDA_TRY(cudaMemsetAsync(counts, 0, 3 * sizeof(int64_t), s));
+    const long long tiles = nb * nb;
+    const int threads = 256;
+    const long long blocks = (tiles + threads - 1) / threads;
+    census_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, s>>>(
+        p->F, p->T, p->W, p->ref, p->N, tile, nb, reinterpret_cast<unsigned long long *>(counts));
+    VDIT_CUDA_TRY(cudaGetLastError());
+    return VDIT_OK;
 }

@@ -31,16 +31,6 @@ __device__ __forceinline__ bool elect_one() {
     return e != 0;
 }
 
-// Warpgroup-wide register reallocation (all 4 warps of a warpgroup execute it).
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -278,22 +268,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for x in [-126, 127]: 2^x = 2^r * 2^f with r = round(x)
-// and f = x - r in [-1/2, 1/2]. The rounding uses the 1.5 * 2^23 addition
-// (the integer lands in the low mantissa bits of t), 2^f is a cubic fitted by
-// weighted least squares for relative error (see gen_exp2_poly.py; max
-// relative error 1.2e-4), and 2^r is applied by adding r to the exponent field.
-// Inputs below -126 are clamped (results there are below 2^-126).
-__device__ __forceinline__ float exp2_fma(float x) {
-    constexpr float kRound = 12582912.0f;     // 1.5 * 2^23
-    constexpr float kC1 = 6.933686137e-01f, kC2 = 2.422178388e-01f, kC3 = 5.459282547e-02f;
-    x = fmaxf(x, -126.0f);
-    const float t = x + kRound;
-    const float f = x - (t - kRound);
-    const float p = fmaf(fmaf(fmaf(kC3, f, kC2), f, kC1), f, 1.0f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 // Packed pairs of fp32 (sm_100+ f32x2 arithmetic: two IEEE round-to-nearest

@@ -58,6 +58,10 @@ typedef enum {
 
 enum { VDIT_O_BF16 = 0, VDIT_O_F32 = 1 };
 enum { VDIT_MODE_AUTO = 0, VDIT_MODE_FORCE_ONLINE = 1, VDIT_MODE_FORCE_STATIC = 2 };
+/* Which part of the mask a plan schedules (vdit_attn_plan_part). */
+enum { VDIT_PART_ALL = 0, VDIT_PART_WINDOW = 1, VDIT_PART_REFERENCE = 2 };
+/* Tiling of the two-pass ablation (vdit_attn_fwd_two_pass). */
+enum { VDIT_TILES_FRAME = 0, VDIT_TILES_128 = 1 };
 
 typedef struct vdit_plan vdit_plan; /* opaque, owned by the library */
 
@@ -79,6 +83,7 @@ typedef struct {
     const int32_t *d_segments;   /* [n_segments][8]: row0, rows, lo0, hi0, lo1, hi1, ntiles, keys */
     const int32_t *d_units;      /* [n_units]: (segment << 16) | tile pair, longest first */
     const int32_t *d_class_off;  /* [n_classes + 1] unit offsets of the cost classes */
+    int32_t part;                /* VDIT_PART_*: the part of the mask this plan schedules */
 } vdit_plan_info;
 
 /* Build the block schedule of the frame-window + reference-frame mask
@@ -97,6 +102,22 @@ typedef struct {
 VDIT_API vdit_status vdit_attn_plan(int32_t num_frames, int32_t tokens_per_frame, int32_t window_radius,
                            int32_t ref_frame, int32_t block_size, void *stream, vdit_plan **out);
 
+/* A plan for one part of the mask, for the two-pass form of the attention that
+ * "Deleting the Mask" describes as the design before frame alignment: the
+ * frame window and the reference frame run as two separate attention passes
+ * whose results a merge pass combines (vdit_attn_fwd_two_pass).
+ *   part = VDIT_PART_ALL: the whole mask, exactly vdit_attn_plan;
+ *   part = VDIT_PART_WINDOW: the frames g with |f - g| <= W only;
+ *   part = VDIT_PART_REFERENCE: the reference frame only, for query frames whose
+ *     window does not contain it (the other frames see no key and get no work).
+ * The two parts partition every query's live keys. Arguments and errors as
+ * vdit_attn_plan; the window and reference parts also need a reference frame
+ * (ref >= 0) and a window that does not cover every frame (W < F-1), else
+ * VDIT_ERR_INVALID. */
+VDIT_API vdit_status vdit_attn_plan_part(int32_t num_frames, int32_t tokens_per_frame,
+                                         int32_t window_radius, int32_t ref_frame, int32_t block_size,
+                                         int32_t part, void *stream, vdit_plan **out);
+
 /* Re-launch the schedule kernels into the plan's existing buffers on `stream`
  * (asynchronous, no allocation, no synchronisation). The contents equal those
  * written by vdit_attn_plan. Errors: VDIT_ERR_INVALID (null plan), VDIT_ERR_CUDA. */
@@ -110,6 +131,19 @@ VDIT_API vdit_status vdit_plan_get_info(const vdit_plan *plan, vdit_plan_info *i
  * expires. *code receives the raw word (0 = none). Returns VDIT_OK when the
  * word was 0, VDIT_ERR_TIMEOUT otherwise. */
 VDIT_API vdit_status vdit_plan_status(vdit_plan *plan, void *stream, int32_t *code);
+
+/* Block census of the plan's mask under a tiling that ignores frames
+ * ("Deleting the Mask": tiles of a multiple of 128 tokens straddle frame
+ * boundaries, and about one live block in five comes out partial). Over the
+ * N x N token pairs cut into tile x tile blocks from token 0 (the last block
+ * of each axis ragged when tile does not divide N), writes to counts[0..2]
+ * (int64, caller-owned DEVICE memory, 8-byte aligned) the number of blocks
+ * whose token pairs are all live, some live, and none live. Partial blocks are
+ * the ones such a kernel must mask element by element; a tile that divides the
+ * frame's token span leaves none. tile: a positive multiple of 16.
+ * Asynchronous on `stream`. Errors: VDIT_ERR_INVALID, VDIT_ERR_CUDA. */
+VDIT_API vdit_status vdit_plan_block_census(const vdit_plan *plan, int32_t tile, int64_t *counts,
+                                            void *stream);
 
 /* Free the plan and its device buffers (synchronous w.r.t. the device). NULL is ignored. */
 VDIT_API void vdit_plan_destroy(vdit_plan *plan);
@@ -171,8 +205,10 @@ VDIT_API vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int32_
  * scale: finite and > 0. o and lse must not share memory with q, k or v (the
  * kernel reads q, k, v tiles while other CTAs write o).
  * k_mean, k_rmax: outputs of vdit_key_stats for the same k. A kernel whose
- * bounded wait expires stops early and sets the plan's status word (see
- * vdit_plan_status). The result is deterministic: two identical calls write
+ * bounded wait expires stops early, leaving O and LSE partly unwritten, and sets
+ * the plan's status word: the call itself returns before the kernel runs and
+ * cannot report it, so check vdit_plan_status after the stream has passed the
+ * call wherever a truncated result must not be used. The result is deterministic: two identical calls write
  * identical bytes. Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
 VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k, const void *v,
                           void *o, int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
@@ -180,6 +216,64 @@ VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const v
                           const int64_t v_strides[3], const int64_t o_strides[3], float scale,
                           const float *k_mean, const float *k_rmax, const uint8_t *eligible,
                           int32_t mode, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The design before frame alignment, kept as an ablation ("Deleting the Mask",
+ * Fig. 3). Before the fix the pages describe, the kernel tiled the sequence in
+ * multiples of 128 that ignore frame boundaries: live blocks straddled frames,
+ * so the blocks that came out partial needed a mask predicate in the inner
+ * loop, and the sequence was padded so that the block grid covered it; and the
+ * frame window and the reference frame ran as two separate attention passes
+ * writing full-precision intermediates that a merge pass re-read. These calls
+ * compute the same attention as vdit_attn_fwd that way, so the cost of each
+ * piece can be measured against the frame-aligned single pass.
+ * ------------------------------------------------------------------------- */
+
+/* vdit_attn_fwd with the frame-blind tiling: query blocks of 256 rows (two
+ * 128-row tiles) and 128-key tiles at fixed multiples of 128 over the sequence
+ * padded to a multiple of 128 (rows and keys beyond N are read as zeros and
+ * never stored). Each block visits every 128-key tile holding a live key of
+ * one of its rows; in a tile where some row of a warp also sees dead keys, each
+ * element of S is tested against that row's live key runs and dead ones are
+ * set to -inf before the softmax. Uses the plan's mask geometry and part (a
+ * plan of vdit_attn_plan_part runs that part alone: rows that see no key of it
+ * get O = 0 and LSE = -inf); its block schedule is not used. Arguments,
+ * outputs, tolerances and errors as vdit_attn_fwd. */
+VDIT_API vdit_status vdit_attn_fwd_tiles128(const vdit_plan *plan, const void *q, const void *k,
+                                            const void *v, void *o, int32_t o_dtype, float *lse,
+                                            int32_t B, int32_t H, int32_t D,
+                                            const int64_t q_strides[3], const int64_t k_strides[3],
+                                            const int64_t v_strides[3], const int64_t o_strides[3],
+                                            float scale, const float *k_mean, const float *k_rmax,
+                                            const uint8_t *eligible, int32_t mode, void *stream);
+
+/* Bytes of device workspace vdit_attn_fwd_two_pass needs: fp32 O and LSE of
+ * both passes, 2 * (B*H*N*D + B*H*N) * 4 bytes (each array 256-byte aligned). */
+VDIT_API size_t vdit_attn_two_pass_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D);
+
+/* The attention of the whole mask in two passes and a merge: pass a runs
+ * plan_window (vdit_attn_plan_part with VDIT_PART_WINDOW), pass b runs
+ * plan_reference (VDIT_PART_REFERENCE of the same F, T, W, ref), each writing
+ * fp32 O and LSE into the workspace; the merge kernel re-reads both and, per
+ * row, with M = max(LSE_a, LSE_b) and w_x = exp(LSE_x - M), writes
+ *   O = (w_a O_a + w_b O_b) / (w_a + w_b),  LSE = M + ln(w_a + w_b)
+ * into o (bf16 or fp32, o_strides) and lse (fp32 [B, H, N] dense, or NULL);
+ * rows whose frame sees no key of pass b take pass a unchanged. Both passes use
+ * the same per-head statistics and mode. tiles = VDIT_TILES_FRAME runs both
+ * passes with the frame-aligned kernel (vdit_attn_fwd), VDIT_TILES_128 with the
+ * frame-blind tiling (vdit_attn_fwd_tiles128). workspace: at least
+ * vdit_attn_two_pass_workspace_size bytes of caller-owned device memory,
+ * 256-byte aligned. Asynchronous on `stream`. Errors: VDIT_ERR_INVALID (plans
+ * that are not the two parts of one mask, workspace, arguments),
+ * VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA, and those of vdit_attn_fwd. */
+VDIT_API vdit_status vdit_attn_fwd_two_pass(const vdit_plan *plan_window, const vdit_plan *plan_reference,
+                                            const void *q, const void *k, const void *v, void *o,
+                                            int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
+                                            const int64_t q_strides[3], const int64_t k_strides[3],
+                                            const int64_t v_strides[3], const int64_t o_strides[3],
+                                            float scale, const float *k_mean, const float *k_rmax,
+                                            const uint8_t *eligible, int32_t mode, int32_t tiles,
+                                            void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of device workspace vdit_key_stats_framed needs for this plan and sizes. */
 VDIT_API size_t vdit_key_stats_framed_workspace_size(const vdit_plan *plan, int32_t B, int32_t H,
@@ -306,19 +400,6 @@ VDIT_API vdit_status vdit_qkv_status(void *workspace, void *stream, int32_t *cod
  * ------------------------------------------------------------------------- */
 typedef struct vdit_pipeline vdit_pipeline;
 
-/* Create a pipeline for attention with `plan` over B x H heads of size D, split
- * into `groups` head groups: group_heads[g] heads each (host array of `groups`
- * positive counts summing to H), or, when group_heads is NULL, ceil(H / groups)
- * heads each (the last may be smaller). groups = 0 with group_heads NULL picks
- * a tapered schedule: 1, 2, 3 heads, then groups of 4 (the heads left over
- * spread one at a time over those groups), then 3, 2, 1 heads, so that the
- * exposed first copy-in and last copy-out are one head each; for H < 16 an
- * even split into groups of about 4. Allocates two device slots (Q, K, V, O,
- * LSE, statistics and their workspace for the largest group each), four streams
- * and the events; owns them until vdit_pipeline_destroy. Errors:
- * VDIT_ERR_INVALID (null plan or out, B or H < 1, groups outside [0, H], bad
- * group_heads, plan from another device), VDIT_ERR_UNSUPPORTED (D),
- * VDIT_ERR_NOMEM, VDIT_ERR_CUDA. */
 /* The head-group schedule that vdit_pipeline_create picks for H heads when
  * groups = 0 and group_heads is NULL: writes the head count of each group to
  * out[0 .. n-1] (host array of cap entries) and returns n, or returns 0 and
@@ -326,6 +407,21 @@ typedef struct vdit_pipeline vdit_pipeline;
  * work, no allocation, callable without a GPU. */
 VDIT_API int32_t vdit_pipeline_default_groups(int32_t H, int32_t *out, int32_t cap);
 
+/* Create a pipeline for attention with `plan` over B x H heads of size D, split
+ * into `groups` head groups: group_heads[g] heads each (host array of `groups`
+ * positive counts summing to H), or, when group_heads is NULL, ceil(H / groups)
+ * heads each (the last may be smaller). groups = 0 with group_heads NULL picks
+ * a tapered schedule: 1, 2, 3 heads, then groups of 4 (the heads left over
+ * spread one at a time over those groups, so a middle group holds up to 7 heads
+ * when there are fewer middle groups than leftover heads, e.g. 1,2,3,7,3,2,1 for
+ * H = 19), then 3, 2, 1 heads, so that the exposed first copy-in and last
+ * copy-out are one head each; for H < 16, and for H >= 248 (where the tapered
+ * schedule would need more than 64 groups), an even split into groups of about 4. Allocates two device slots (Q, K, V, O,
+ * LSE, statistics and their workspace for the largest group each), four streams
+ * and the events; owns them until vdit_pipeline_destroy. Errors:
+ * VDIT_ERR_INVALID (null plan or out, B or H < 1, groups outside [0, H], bad
+ * group_heads, plan from another device), VDIT_ERR_UNSUPPORTED (D),
+ * VDIT_ERR_NOMEM, VDIT_ERR_CUDA. */
 VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int32_t H, int32_t D,
                                           int32_t groups, const int32_t *group_heads,
                                           vdit_pipeline **out);
@@ -339,14 +435,20 @@ VDIT_API vdit_status vdit_pipeline_create(const vdit_plan *plan, int32_t B, int3
  * `stream`, and `stream` waits for all of it, so a synchronisation of `stream`
  * means o_host (and lse_host) are complete; every host buffer stays owned by
  * the caller and must stay valid until then. An expired wait inside attention
- * is reported by vdit_plan_status on the plan. Arguments (pointers, strides,
- * scale finite and > 0, tau >= 0, mode) are checked before anything is queued.
+ * is reported only by vdit_plan_status on the plan: this call cannot see it (the
+ * kernels run after it returns), so a caller that must not use a truncated O
+ * calls vdit_plan_status after the stream has passed the run. Arguments
+ * (pointers, strides, scale finite and > 0, tau >= 0, mode) are checked before
+ * anything is queued.
  * Consecutive batches overlap when they run on two pipelines, each with its
  * own plan, on two streams: one batch's first copy-in and last copy-out then
  * run beside the other batch's kernels (+6% at the 720p-like shape).
  * An error from a later step returns at once; copies and kernels of earlier
- * groups may still be in flight, and the host buffers must stay valid until
- * `stream` (or the device) is synchronised. Errors: VDIT_ERR_INVALID,
+ * groups may still be in flight, and `stream` is made to wait for all of them,
+ * so the host buffers must stay valid until `stream` is synchronised, as on
+ * success. A pipeline may be driven from different streams in turn: a run
+ * reuses a device slot only after the previous run's kernels and copies of that
+ * slot are done. Errors: VDIT_ERR_INVALID,
  * VDIT_ERR_CUDA, and those of vdit_key_stats and vdit_attn_fwd. */
 VDIT_API vdit_status vdit_pipeline_run(vdit_pipeline *pipeline, const void *q_host,
                                        const void *k_host, const void *v_host, void *o_host,
@@ -374,6 +476,14 @@ VDIT_API void vdit_set_wait_limit_ns(uint64_t ns);
  * made it frees what it had allocated and returns VDIT_ERR_NOMEM. n <= 0
  * switches the hook off. For tests of the error paths; no fault is involved. */
 VDIT_API void vdit_set_alloc_fail_after(int32_t n);
+
+/* Launch-failure test hook. With n >= 1, the n-th attention launch from now on
+ * (vdit_attn_fwd, vdit_attn_fwd_framed, and those inside vdit_pipeline_run;
+ * counted process-wide) is refused before anything is launched, once, as if
+ * the launch had failed: the call returns VDIT_ERR_CUDA. n <= 0 switches the
+ * hook off. For tests of the error paths (e.g. a pipeline run that fails part-
+ * way); no fault is involved. */
+VDIT_API void vdit_set_launch_fail_after(int32_t n);
 
 /* Thread-local, library-owned text of the last error on this thread ("" if none). */
 VDIT_API const char *vdit_last_error(void);

@@ -120,3 +120,25 @@ def test_plan_at_the_frame_limit():
     assert sorted(ukeys.tolist(), reverse=True) == sorted(keys, reverse=True)
     cls = plan.class_offsets().cpu().numpy()
     assert len(cls) - 1 == len(set(keys))
+
+
+CENSUS = [
+    (9, 400, 1, 0, 80, 128), (9, 400, 1, 0, 80, 80),        # small: 128-tiles vs a divisor
+    (4, 48, 1, 0, 16, 128), (4, 48, 1, 0, 16, 16),           # tiny
+    (13, 3600, 2, 0, 240, 128), (13, 3600, 2, 0, 240, 1024),  # 720p-like
+    (9, 8160, 1, 0, 240, 128), (9, 8160, 1, 0, 240, 1024),    # 1080p-like
+    (21, 1560, 20, 0, 16, 128),                               # dense: every block live
+    (3, 48, 0, 0, 16, 32), (2, 48, 0, -1, 16, 32), (7, 144, 1, 3, 48, 256),
+]
+
+
+@pytest.mark.parametrize("F,T,W,ref,bs,tile", CENSUS)
+def test_block_census_bit_exact(F, T, W, ref, bs, tile):
+    """Partial blocks under a frame-blind tiling ("Deleting the Mask": about one
+    live block in five partial under 128-multiple tiles), counted on the device,
+    equal the oracle's token-by-token count."""
+    plan = vd.attn_plan(F, T, W, ref, bs)
+    got = plan.block_census(tile)
+    assert got == oracle.block_census(F, T, W, ref, tile)
+    if T % tile == 0:
+        assert got[1] == 0

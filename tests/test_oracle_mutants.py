@@ -41,6 +41,10 @@ MUTANTS = [
     ("second_run_dropped", "runs[4 * f + 3] = nr > 1 ? (int32_t)hi[1] : 0;",
      "runs[4 * f + 3] = nr > 1 ? (int32_t)lo[1] : 0;", [SCHED]),
     ("pairs_count_blocks", "pairs += cnt;", "pairs += cnt > 0;", [SCHED]),
+    # block census (partial blocks under tiles that straddle frames)
+    ("census_ragged_tile_full_area", "int64_t area = (i1 - i0) * (j1 - j0);",
+     "int64_t area = (int64_t)bs * bs;", [SCHED]),
+    ("census_partial_as_full", "if (live == area)", "if (live * 2 >= area)", [SCHED]),
     # exact bf16 reading
     ("bf16_read_rounded", "uint32_t u = ((uint32_t)((const uint16_t *)p)[idx]) << 16;",
      "uint32_t u = (((uint32_t)((const uint16_t *)p)[idx]) << 16) | 0x8000u;", [ATTN]),

@@ -93,12 +93,56 @@ def test_schedule_csr_and_runs(F, T, W, ref):
             assert list(s.runs[f]) == want
 
 
+def frame_level_census(F, T, W, ref, tile):
+    """(full, partial, dead) tile x tile blocks from the frame adjacency alone: a
+    block's token pairs are all live when every (query frame, key frame) pair it
+    covers is adjacent, none when no pair is. Independent of the oracle's
+    token-by-token count."""
+    adj = frame_adjacency(F, W, ref)
+    N = F * T
+    edges = [(i0, min(i0 + tile, N)) for i0 in range(0, N, tile)]
+    span = [(a // T, (b - 1) // T) for a, b in edges]
+    counts = [0, 0, 0]
+    for fa, fb in span:
+        for ga, gb in span:
+            sub = adj[fa:fb + 1, ga:gb + 1]
+            counts[0 if sub.all() else (1 if sub.any() else 2)] += 1
+    return tuple(counts)
+
+
+def test_block_census_hand_counts():
+    """Hand-derived censuses ("Deleting the Mask": tiles that straddle frame
+    boundaries come out partial).
+    (a) Two frames of 48 tokens, block-diagonal mask (W = 0, no reference), 32-token
+        tiles: tiles 0 and 2 lie inside one frame each, tile 1 straddles both; the
+        diagonal tiles (0,0) and (2,2) are full, (0,2) and (2,0) dead, the five
+        pairs touching tile 1 partial.
+    (b) Three frames of 48, W = 0, reference frame 0, 32-token tiles (the last one
+        16 tokens): per query tile the counts are (1,1,3), (1,2,2), (3,0,2),
+        (3,1,1), (3,1,1) as (full, partial, dead)."""
+    assert oracle.block_census(2, 48, 0, -1, 32) == (2, 5, 2)
+    assert oracle.block_census(3, 48, 0, 0, 32) == (11, 5, 9)
+
+
+@pytest.mark.parametrize("F,T,W,ref,tile", [
+    (9, 400, 1, 0, 128), (9, 400, 1, 0, 80), (4, 48, 1, 0, 128), (13, 120, 2, 0, 128),
+    (13, 120, 2, 0, 1024), (7, 144, 1, 3, 256), (6, 160, 0, -1, 128), (21, 104, 20, 0, 128),
+    (5, 37 * 16, 1, 4, 48),
+])
+def test_block_census_matches_frame_level_construction(F, T, W, ref, tile):
+    got = oracle.block_census(F, T, W, ref, tile)
+    assert got == frame_level_census(F, T, W, ref, tile)
+    assert sum(got) == (-(-F * T // tile)) ** 2
+
+
 def test_misaligned_blocks_are_partial():
     """Blocks of 128 tokens over frames whose token count 128 does not divide mix
-    live and dead token pairs ("Deleting the Mask"): 128-token blocks over 400-token frames leave partial blocks, a
-    divisor of the span leaves none."""
+    live and dead token pairs ("Deleting the Mask"): 128-token blocks over
+    400-token frames leave partial blocks (the exact count from the frame-level
+    construction), a divisor of the span leaves none."""
     F, T, W, ref = 9, 400, 1, 0
     full, partial, dead = oracle.block_census(F, T, W, ref, 128)
+    assert (full, partial, dead) == frame_level_census(F, T, W, ref, 128)
     assert partial > 0
     with pytest.raises(ValueError):
         oracle.schedule(F, T, W, ref, 128)
