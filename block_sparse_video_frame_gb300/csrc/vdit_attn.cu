@@ -648,64 +648,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (j >= 2) mbar_arrive(bar(kBarVfree + (kc0 + j - 2) % kStagesV));
                     if (j == u.nkt - 1) mbar_arrive(bar(kBarQfree));
                 }
-                // the whole 128-column S row in one TMEM load
-                uint32_t v[128];
-                tmem_ld128(tS, v);
-                if constexpr (kTiled) {
-                    // a tile that straddles a frame boundary: the mask predicate, per
-                    // element, turns this row's dead keys (and padding) into -inf
-                    const bool full = (rlo0 <= start && start + kBK <= rhi0) ||
-                                      (rlo1 <= start && start + kBK <= rhi1);
-                    if (!__all_sync(0xffffffffu, full)) {
-#pragma unroll
-                        for (int e = 0; e < 128; ++e) {
-                            const int jk = start + e;
-                            const bool live = (unsigned)(jk - rlo0) < (unsigned)(rhi0 - rlo0) ||
-                                              (unsigned)(jk - rlo1) < (unsigned)(rhi1 - rlo1);
-                            v[e] = live ? v[e] : 0xff800000u;
-                        }
-                    }
-                }
-                float mrow = mt;
-                float alpha = 1.f;      // online: factor of the O rescale (lazy, warp-uniform)
-                bool rescale = false;
-                if (!stat) {
-                    // online: this tile's row max, taken on the raw logits (the scale
-                    // is positive), then the lazy rescale decision
-                    float mx;
-                    if (nvalid >= kBK) {
-                        float m8[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(v[e]);
-#pragma unroll
-                        for (int e = 8; e < 128; ++e) m8[e % 8] = fmaxf(m8[e % 8], __uint_as_float(v[e]));
-                        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                    } else {
-                        mx = -INFINITY;
-#pragma unroll
-                        for (int e = 0; e < 128; ++e) mx = e < nvalid ? fmaxf(mx, __uint_as_float(v[e])) : mx;
-                    }
-                    mx *= sc;
-                    if (j == j0) {
-                        mrun = mx;
-                    } else {
-                        const bool need = mx > mrun + kLazyRescale;
-                        if (__any_sync(0xffffffffu, need)) {
-                            rescale = true;
-                            alpha = need ? ex2(mrun - mx) : 1.f;
-                            l0 *= alpha;
-                            l1 *= alpha;
-                            if (need) mrun = mx;
-                        }
-                    }
-                    mrow = mrun;
-                    // no live key in this row yet (frame-blind tiling): every term is
-                    // masked, any finite shift gives p = 0
-                    if constexpr (kTiled) mrow = mrow == -INFINITY ? 0.f : mrow;
-                }
-                // p = 2^(s*scale*log2e - m~), P -> bf16 into the first half of S
-                {
+                // p = 2^(s*scale*log2e - mrow), P -> bf16 into the first half of S, from
+                // the 128-column S row in registers
+                auto exps = [&](uint32_t (&v)[128], float mrow) {
                     const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-mrow, -mrow);
                     uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -743,17 +688,82 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     f2_unpack(l2, a0, a1);
                     l0 += a0;
                     l1 += a1;
-                }
-                if (rescale) {
-                    // O (after P.V of the previous key tile, which the S barrier of this
-                    // tile covers) scaled to the new running max, before this tile's P.V
+                };
+                // frame-blind tiling: in a tile that straddles a frame boundary the mask
+                // predicate, per element, turns this row's dead keys (and padding) into -inf
+                auto mask = [&](uint32_t (&v)[128]) {
+                    if constexpr (kTiled) {
+                        const bool full = (rlo0 <= start && start + kBK <= rhi0) ||
+                                          (rlo1 <= start && start + kBK <= rhi1);
+                        if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c0, o);
+                            for (int e = 0; e < 128; ++e) {
+                                const int jk = start + e;
+                                const bool live = (unsigned)(jk - rlo0) < (unsigned)(rhi0 - rlo0) ||
+                                                  (unsigned)(jk - rlo1) < (unsigned)(rhi1 - rlo1);
+                                v[e] = live ? v[e] : 0xff800000u;
+                            }
+                        }
+                    }
+                };
+                // Each path loads the whole S row in one TMEM load of its own: a load
+                // shared by both paths ahead of the branch measured 8% slower on the
+                // static path.
+                if (stat) {
+                    uint32_t v[128];
+                    tmem_ld128(tS, v);
+                    mask(v);
+                    exps(v, mt);
+                } else {
+                    uint32_t v[128];
+                    tmem_ld128(tS, v);
+                    mask(v);
+                    // online: this tile's row max, taken on the raw logits (the scale is
+                    // positive), then the lazy rescale decision
+                    float mx;
+                    if (nvalid >= kBK) {
+                        float m8[8];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + c0, o);
+                        for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(v[e]);
+#pragma unroll
+                        for (int e = 8; e < 128; ++e) m8[e % 8] = fmaxf(m8[e % 8], __uint_as_float(v[e]));
+                        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    } else {
+                        mx = -INFINITY;
+#pragma unroll
+                        for (int e = 0; e < 128; ++e) mx = e < nvalid ? fmaxf(mx, __uint_as_float(v[e])) : mx;
+                    }
+                    mx *= sc;
+                    float alpha = 1.f;      // factor of the O rescale (lazy, warp-uniform)
+                    bool rescale = false;
+                    if (j == j0) {
+                        mrun = mx;
+                    } else {
+                        const bool need = mx > mrun + kLazyRescale;
+                        if (__any_sync(0xffffffffu, need)) {
+                            rescale = true;
+                            alpha = need ? ex2(mrun - mx) : 1.f;
+                            l0 *= alpha;
+                            l1 *= alpha;
+                            if (need) mrun = mx;
+                        }
+                    }
+                    // no live key in this row yet (frame-blind tiling): every term is
+                    // masked, any finite shift gives p = 0
+                    exps(v, kTiled && mrun == -INFINITY ? 0.f : mrun);
+                    if (rescale) {
+                        // O (after P.V of the previous key tile, which the S barrier of
+                        // this tile covers) scaled to the new running max, before this
+                        // tile's P.V
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c0, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c0, o);
+                        }
                     }
                 }
                 tmem_wait_st();
