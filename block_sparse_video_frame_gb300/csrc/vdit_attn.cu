@@ -193,18 +193,13 @@ __device__ __forceinline__ void decode(const Params &p, long long w, Work &u) {
 // the reference frame (each rounded out to 128 keys); tiles where a row also
 // sees dead keys are masked element by element in the softmax. Row i of the
 // padded tail (i >= N) is computed as a row of the last frame and not stored.
-// Blocks walk the heads two at a time in sequence order.
+// Blocks walk the heads in order, each head's blocks in sequence order.
 __device__ __forceinline__ void decode_tiled(const Params &p, long long w, Work &u) {
-    const int BH = p.B * p.H;
     const long long per_head = p.n_blocks;
-    const long long g = w / (per_head * kHeadGroup);
-    const int gh = min(kHeadGroup, BH - (int)g * kHeadGroup);
-    w -= g * per_head * kHeadGroup;
-    u.bh = (int)(g * kHeadGroup + w / per_head);
+    u.bh = (int)(w / per_head);          // heads in order, blocks in sequence order inside a head
     const int blk = (int)(w % per_head);
     u.b = u.bh / p.H;
     u.h = u.bh % p.H;
-    (void)gh;
     const int npad = (p.N + kBK - 1) / kBK * kBK;
     u.seg = 0;
     u.pair = 0;

@@ -159,37 +159,36 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_run
     *hdr = h;
 }
 
+// One warp per query block: the lanes sum the blocks of the earlier frames (the
+// row's offset) and write the row's key blocks, 32 at a time.
 __global__ void plan_csr_kernel(PlanArgs a, const int32_t *frame_runs, int32_t *row_ptr,
                                 int32_t *col_idx) {
-    const int qb = blockIdx.x * blockDim.x + threadIdx.x;
+    const int qb = (int)((blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32);
+    const int lane = threadIdx.x % 32;
     if (qb >= a.nqb) return;
-    long long start;
+    long long start, len;
     if (a.dense) {
         start = (long long)qb * a.nqb;
-        for (int kb = 0; kb < a.nqb; ++kb) col_idx[start + kb] = kb;
+        len = a.nqb;
+        for (int kb = lane; kb < a.nqb; kb += 32) col_idx[start + kb] = kb;
     } else {
         const int per = a.T / a.bs;
         const int f = qb / per;
         long long before = 0;
-        for (int g = 0; g < f; ++g) {
+        for (int g = lane; g < f; g += 32) {
             const int32_t *r = frame_runs + 4 * g;
             before += (long long)((r[1] - r[0]) + (r[3] - r[2])) / a.bs;
         }
+        for (int o = 16; o > 0; o /= 2) before += __shfl_xor_sync(0xffffffffu, before, o);
         const int32_t *r = frame_runs + 4 * f;
-        const int row_len = ((r[1] - r[0]) + (r[3] - r[2])) / a.bs;
-        start = before * per + (long long)(qb - f * per) * row_len;
-        long long k = start;
-        for (int run = 0; run < 2; ++run) {
-            for (int kb = r[2 * run] / a.bs; kb < r[2 * run + 1] / a.bs; ++kb) col_idx[k++] = kb;
-        }
+        const int n0 = (r[1] - r[0]) / a.bs, k0 = r[0] / a.bs, k1 = r[2] / a.bs;
+        len = n0 + (r[3] - r[2]) / a.bs;
+        start = before * per + (long long)(qb - f * per) * len;
+        for (int i = lane; i < len; i += 32) col_idx[start + i] = i < n0 ? k0 + i : k1 + (i - n0);
     }
-    row_ptr[qb] = (int32_t)start;
-    if (qb == a.nqb - 1) {
-        long long len = a.dense ? a.nqb
-                                : ((frame_runs[4 * (a.F - 1) + 1] - frame_runs[4 * (a.F - 1)]) +
-                                   (frame_runs[4 * (a.F - 1) + 3] - frame_runs[4 * (a.F - 1) + 2])) /
-                                      a.bs;
-        row_ptr[a.nqb] = (int32_t)(start + len);
+    if (lane == 0) {
+        row_ptr[qb] = (int32_t)start;
+        if (qb == a.nqb - 1) row_ptr[a.nqb] = (int32_t)(start + len);
     }
 }
 
@@ -257,8 +256,7 @@ cudaError_t launch_plan_kernels(const vdit_plan *p, cudaStream_t stream, bool cs
                                              p->d_units, p->d_class_off);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !csr) return e;
-    plan_csr_kernel<<<(a.nqb + 255) / 256, 256, 0, stream>>>(a, p->d_frame_runs, p->d_row_ptr,
-                                                             p->d_col_idx);
+    plan_csr_kernel<<<(a.nqb + 7) / 8, 256, 0, stream>>>(a, p->d_frame_runs, p->d_row_ptr, p->d_col_idx);
     return cudaGetLastError();
 }
 

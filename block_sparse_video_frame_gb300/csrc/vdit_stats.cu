@@ -8,7 +8,7 @@
 //   c    = (1/N) sum_j k_j          R  = max_j |k_j - c|
 //   Qm   = max_i |q_i|              G  = 2 * scale * Qm * R,  eligible = G <= tau
 // HBM-bound: K is read twice (the second read comes from L2 only while K fits
-// there; at 720p it does not), Q once.
+// there; at 720p only the last heads of the first pass are still there), Q once.
 // Four launches, every reduction in a fixed order (bitwise reproducible):
 //   stats_pass1    per chunk of 512 rows: column sums of K, max |q|^2
 //   stats_mean     c = (sum of the chunk column sums) / N, per head
@@ -155,7 +155,10 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
     constexpr int LPR = D / 8;
     constexpr int RPW = 32 / LPR;
     __shared__ float s_r[kStatsWarps];
-    const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+    // Heads in reverse order: pass 1 walked them forward, so the keys of its last
+    // heads are still in L2 when this pass starts (each head's result is the same in
+    // any order).
+    const int chunk = blockIdx.x, bh = a.B * a.H - 1 - blockIdx.y, b = bh / a.H, h = bh % a.H;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int sub = lane / LPR, col = (lane % LPR) * 8;
     float cm[8];
