@@ -71,10 +71,19 @@ __device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_fram
     r[0] = lo0; r[1] = hi0; r[2] = lo1; r[3] = hi1;
 }
 
-__global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_runs,
-                                 int32_t *segments, int32_t *units, int32_t *class_off) {
+// One block. The frames' runs are computed in parallel; one thread then builds
+// the segments, sorts them and lays out the cost classes, with every
+// intermediate in shared memory (the runs of a frame are recomputed, not read
+// back); the unit list is written by all threads.
+__global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32_t *__restrict__ frame_runs,
+                                 int32_t *__restrict__ segments, int32_t *__restrict__ units,
+                                 int32_t *__restrict__ class_off) {
+    // s_cnt: live frames per frame, then per segment its key count, then its first unit.
+    // s_order: segments longest first, each entry (tile pairs << 12) | segment.
     __shared__ int s_cnt[kMaxFrames];
     __shared__ int s_order[kMaxFrames];
+    __shared__ int s_nused;   // segments that get units (in s_order)
+    static_assert(kMaxFrames <= (1 << 12), "segment index field of s_order");
     for (int f = threadIdx.x; f < a.F; f += blockDim.x) {
         int r[4], live;
         frame_runs_of(a, f, r, live);
@@ -85,78 +94,87 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *hdr, int32_t *frame_run
         s_cnt[f] = live;
     }
     __syncthreads();
-    if (threadIdx.x != 0) return;
-
-    PlanHeader h{};
-    // counts ------------------------------------------------------------
-    long long fp = 0;
-    for (int f = 0; f < a.F; ++f) fp += s_cnt[f];
-    h.live_pairs = fp * (long long)a.T * a.T;
-    if (a.dense) {
-        h.nnz = (long long)a.nqb * a.nqb;
-    } else {
-        long long per = a.T / a.bs;
-        h.nnz = fp * per * per;
-    }
-    // segments: consecutive frames with identical run lists --------------
-    int nseg = 0;
-    for (int f = 0; f < a.F; ++f) {
-        const int32_t *r = frame_runs + 4 * f;
-        bool same = false;
-        if (f > 0) {
-            const int32_t *p = frame_runs + 4 * (f - 1);
-            same = p[0] == r[0] && p[1] == r[1] && p[2] == r[2] && p[3] == r[3];
-        }
-        if (same) {
-            int32_t *s = segments + kSegInts * (nseg - 1);
-            s[1] += a.T;
+    if (threadIdx.x == 0) {
+        PlanHeader h{};
+        // counts ------------------------------------------------------------
+        long long fp = 0;
+        for (int f = 0; f < a.F; ++f) fp += s_cnt[f];
+        h.live_pairs = fp * (long long)a.T * a.T;
+        if (a.dense) {
+            h.nnz = (long long)a.nqb * a.nqb;
         } else {
-            int32_t *s = segments + kSegInts * nseg;
-            s[0] = (int)((long long)f * a.T);
-            s[1] = a.T;
-            s[2] = r[0]; s[3] = r[1]; s[4] = r[2]; s[5] = r[3];
-            s[7] = (r[1] - r[0]) + (r[3] - r[2]);
+            long long per = a.T / a.bs;
+            h.nnz = fp * per * per;
+        }
+        // segments: consecutive frames with identical run lists --------------
+        int nseg = 0, cur[4] = {0, 0, 0, 0}, row0 = 0, rows = 0;
+        auto flush = [&]() {
+            int32_t *g = segments + kSegInts * nseg;
+            const int ntile = (rows + kTileRows - 1) / kTileRows;
+            const int keys = (cur[1] - cur[0]) + (cur[3] - cur[2]);
+            const int npairs = (ntile + kTilesPerUnit - 1) / kTilesPerUnit;
+            g[0] = row0; g[1] = rows;
+            g[2] = cur[0]; g[3] = cur[1]; g[4] = cur[2]; g[5] = cur[3];
+            g[6] = ntile; g[7] = keys;
+            // a unit code keeps the tile pair in its low 16 bits
+            if (npairs > kMaxPairsPerSegment) h.error = 4;
+            s_cnt[nseg] = keys;        // frame counts are no longer needed
+            s_order[nseg] = (min(npairs, kMaxPairsPerSegment) << 12) | nseg;
             ++nseg;
+        };
+        for (int f = 0; f < a.F; ++f) {
+            int r[4], live;
+            frame_runs_of(a, f, r, live);
+            if (f > 0 && r[0] == cur[0] && r[1] == cur[1] && r[2] == cur[2] && r[3] == cur[3]) {
+                rows += a.T;
+                continue;
+            }
+            if (f > 0) flush();
+            cur[0] = r[0]; cur[1] = r[1]; cur[2] = r[2]; cur[3] = r[3];
+            row0 = (int)((long long)f * a.T);
+            rows = a.T;
         }
-    }
-    for (int s = 0; s < nseg; ++s) {
-        int32_t *g = segments + kSegInts * s;
-        g[6] = (g[1] + kTileRows - 1) / kTileRows;
-        s_order[s] = s;
-        // a unit code keeps the tile pair in its low 16 bits
-        if ((g[6] + kTilesPerUnit - 1) / kTilesPerUnit > kMaxPairsPerSegment) h.error = 4;
-    }
-    if (h.error != 0) nseg = 0;
-    // longest first (stable insertion sort on key count) ------------------
-    for (int i = 1; i < nseg; ++i) {
-        int v = s_order[i], key = segments[kSegInts * v + 7], j = i - 1;
-        while (j >= 0 && segments[kSegInts * s_order[j] + 7] < key) {
-            s_order[j + 1] = s_order[j];
-            --j;
+        flush();
+        if (h.error != 0) nseg = 0;
+        // longest first (stable insertion sort on key count) ------------------
+        for (int i = 1; i < nseg; ++i) {
+            const int v = s_order[i], key = s_cnt[v & 0xFFF];
+            int j = i - 1;
+            while (j >= 0 && s_cnt[s_order[j] & 0xFFF] < key) {
+                s_order[j + 1] = s_order[j];
+                --j;
+            }
+            s_order[j + 1] = v;
         }
-        s_order[j + 1] = v;
-    }
-    int nu = 0, ncls = 0, prev_key = -1;
-    for (int i = 0; i < nseg; ++i) {
-        int s = s_order[i];
-        const int32_t *g = segments + kSegInts * s;
-        if (g[7] == 0) break;   // frames that see no key (reference part only): no work, sorted last
-        if (g[7] != prev_key) {
-            if (ncls >= kMaxClasses) { h.error = 2; break; }
-            class_off[ncls++] = nu;
-            prev_key = g[7];
+        // cost classes and the first unit of each segment ---------------------
+        int nu = 0, ncls = 0, prev_key = -1, used = 0;
+        for (int i = 0; i < nseg; ++i) {
+            const int v = s_order[i], sg = v & 0xFFF, np = v >> 12, key = s_cnt[sg];
+            if (key == 0) break;   // frames that see no key (reference part only): no work, sorted last
+            if (key != prev_key) {
+                if (ncls >= kMaxClasses) { h.error = 2; break; }
+                class_off[ncls++] = nu;
+                prev_key = key;
+            }
+            if (nu + np > a.units_cap) { h.error = 3; break; }
+            s_cnt[sg] = nu;
+            nu += np;
+            ++used;
         }
-        int npairs = (g[6] + kTilesPerUnit - 1) / kTilesPerUnit;
-        for (int p = 0; p < npairs; ++p) {
-            if (nu >= a.units_cap) { h.error = 3; break; }
-            units[nu++] = (s << 16) | p;
-        }
+        class_off[ncls] = nu;
+        h.n_segments = nseg;
+        h.n_units = nu;
+        h.n_classes = ncls;
+        *hdr = h;
+        s_nused = used;
     }
-    class_off[ncls] = nu;
-    h.n_segments = nseg;
-    h.n_units = nu;
-    h.n_classes = ncls;
-    *hdr = h;
+    __syncthreads();
+    // units: (segment << 16) | tile pair, in the order of s_order ------------
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+    for (int i = warp; i < s_nused; i += nwarps) {
+        const int v = s_order[i], sg = v & 0xFFF, np = v >> 12, first = s_cnt[sg];
+        for (int p = lane; p < np; p += 32) units[first + p] = (sg << 16) | p;
+    }
 }
 
 // One warp per query block: the lanes sum the blocks of the earlier frames (the
