@@ -150,8 +150,12 @@ __global__ void stats_mean(StatsArgs a, int D) {
     }
 }
 
+// Pass 2 reads one tensor where pass 1 reads two: twice the unroll keeps as many
+// 16-byte loads in flight per warp, packed until used.
+constexpr int kUnroll2 = 2 * kUnroll;
+
 template <int D>
-__global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
+__global__ void __launch_bounds__(kStatsThreads, 4) stats_pass2(StatsArgs a) {
     constexpr int LPR = D / 8;
     constexpr int RPW = 32 / LPR;
     __shared__ float s_r[kStatsWarps];
@@ -170,27 +174,25 @@ __global__ void __launch_bounds__(kStatsThreads) stats_pass2(StatsArgs a) {
     const int r1 = min((fr + 1) * a.T, r0 + kRowsPerChunk);
     constexpr int kStep = kStatsWarps * RPW;
     float rm2 = 0.f;
-    for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll) {
-        float xk[kUnroll][8];
+    for (int wbase = r0 + warp * RPW; wbase < r1; wbase += kStep * kUnroll2) {
+        uint4 xk[kUnroll2];
+        bool in[kUnroll2];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kUnroll2; ++u) {
             const int r = wbase + sub + u * kStep;
-            if (r < r1) {
-                load8(kb + (long long)r * a.ks2, xk[u]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xk[u][e] = cm[e];   // contributes 0
-            }
+            in[u] = r < r1;
+            xk[u] = in[u] ? load16(kb + (long long)r * a.ks2) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kUnroll2; ++u) {
             float sq = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float t = xk[u][e] - cm[e];
+                const float t = elem8(xk[u], e) - cm[e];
                 sq = fmaf(t, t, sq);
             }
-            rm2 = fmaxf(rm2, row_sum<LPR>(sq));
+            sq = row_sum<LPR>(sq);
+            rm2 = in[u] ? fmaxf(rm2, sq) : rm2;   // rows past the chunk contribute nothing
         }
     }
     rm2 = warp_max(rm2);

@@ -132,7 +132,8 @@ VDIT_API vdit_status vdit_plan_get_info(const vdit_plan *plan, vdit_plan_info *i
  * word was 0, VDIT_ERR_TIMEOUT otherwise. */
 VDIT_API vdit_status vdit_plan_status(vdit_plan *plan, void *stream, int32_t *code);
 
-/* Block census of the plan's mask under a tiling that ignores frames
+/* Block census of the plan's whole mask (all parts, whatever part the plan
+ * schedules) under a tiling that ignores frames
  * ("Deleting the Mask": tiles of a multiple of 128 tokens straddle frame
  * boundaries, and about one live block in five comes out partial). Over the
  * N x N token pairs cut into tile x tile blocks from token 0 (the last block
