@@ -168,3 +168,33 @@ def test_default_head_groups_cover_every_head(lib):
     buf = (ctypes.c_int32 * 2)()
     assert lib.vdit_pipeline_default_groups(24, ctypes.cast(buf, ctypes.c_void_p), 2) == 0
     assert lib.vdit_pipeline_default_groups(0, ctypes.cast(buf, ctypes.c_void_p), 2) == 0
+
+
+def test_plan_part_rejects_bad_arguments(lib):
+    """Plans of one mask part (the two-pass ablation): an unknown part, a mask
+    without a reference frame, and a window that covers every frame are refused
+    on the host."""
+    h = ctypes.c_void_p(1234)
+    for args, needle in (((9, 400, 1, 0, 80, 3), "part"), ((9, 400, 1, 0, 80, -1), "part"),
+                         ((9, 400, 1, -1, 80, 2), "no reference frame"),
+                         ((5, 48, 4, 0, 16, 1), "covers every frame")):
+        st = lib.vdit_attn_plan_part(*args, None, ctypes.byref(h))
+        assert st == vd.VDIT_ERR_INVALID, args
+        assert needle in lib.vdit_last_error().decode(), (args, lib.vdit_last_error())
+        assert not h.value
+
+
+def test_ablation_and_census_entry_points_check_arguments(lib):
+    p = ctypes.c_void_p(0x1000)
+    s3 = vd._I64x3(8 * 128, 128 * 16, 128)
+    assert lib.vdit_plan_block_census(None, 128, p, None) == vd.VDIT_ERR_INVALID
+    # two passes need both plans; the workspace size covers fp32 O and LSE of both passes
+    args = [None, None, p, p, p, p, 0, None, 1, 2, 128, s3, s3, s3, s3, 0.1, p, p, p, 0, 0, p, 0, None]
+    assert lib.vdit_attn_fwd_two_pass(*args) == vd.VDIT_ERR_INVALID
+    B, H, N, D = 1, 2, 300, 128
+    al = lambda x: (x + 255) // 256 * 256
+    assert lib.vdit_attn_two_pass_workspace_size(B, H, N, D) == 2 * (al(B * H * N * D * 4) + al(B * H * N * 4))
+    assert lib.vdit_attn_two_pass_workspace_size(0, H, N, D) == 0
+    assert lib.vdit_attn_fwd_tiles128(None, p, p, p, p, 0, None, 1, 2, 128, s3, s3, s3, s3, 0.1, p, p, p, 0,
+                                      None) == vd.VDIT_ERR_INVALID
+    lib.vdit_set_launch_fail_after(0)

@@ -157,3 +157,29 @@ def test_pipeline_rejects_bad_scalars_before_queuing():
     o_ref, _ = device_reference(w, q, k, v, plan)
     assert torch.equal(o_h.view(torch.int16), o_ref.view(torch.int16))
     pipe.close()
+
+
+def test_pipeline_driven_from_two_streams_in_turn():
+    """One pipeline run on stream A and, with no synchronisation in between, again on
+    stream B with other host buffers (the 720p-like geometry, 4 heads, groups of one
+    head, so the second run's first copies would land in slots the first run's
+    kernels still read): a run reuses a device slot only after the previous run's
+    kernels and copies of that slot are done, so both outputs equal their single
+    launches bit for bit."""
+    w = configs.SR720.with_(name="sr720p_h4", H=4, outlier_heads=(3,))
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    ins = [synth.make_qkv(w, seed=s) for s in (5, 6)]
+    refs = [device_reference(w, *x, plan)[0] for x in ins]
+    hosts = [tuple(t.pin_memory() for t in x) for x in ins]
+    outs = [pinned_like(ins[0][0]) for _ in range(2)]
+    pipe = vd.Pipeline(plan, w.B, w.H, w.D, 4)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for i in range(2):
+        pipe.run(*hosts[i], outs[i], w.scale, stream=streams[i], check=False)
+    for s in streams:
+        s.synchronize()
+    assert plan.status() == 0
+    for i in range(2):
+        assert torch.equal(outs[i].view(torch.int16), refs[i].view(torch.int16)), i
+    pipe.close()
