@@ -31,6 +31,9 @@ CASES = [
                      outlier_heads=(1,), seed=18),
     configs.Workload("w2_t640", B=1, H=2, D=128, F=9, T=640, W=2, ref=0, block_size=128,
                      outlier_heads=(1,), seed=22),   # T a multiple of 128: no partial tile
+    # 320 tokens: three 128-row tiles, so the last frame-blind block is a lone tile
+    configs.Workload("lone_block", B=2, H=2, D=128, F=4, T=80, W=1, ref=2, block_size=16,
+                     outlier_heads=(0,), seed=25),
 ]
 
 
@@ -47,7 +50,12 @@ def _plans(w):
 @pytest.mark.parametrize("w", CASES + [configs.DENSE.with_(name="dense_small", F=5, T=104, H=2,
                                                           outlier_heads=(1,), seed=23),
                                        configs.Workload("noref", B=1, H=2, D=128, F=6, T=160, W=0,
-                                                        ref=-1, block_size=32, outlier_heads=(1,), seed=11)],
+                                                        ref=-1, block_size=32, outlier_heads=(1,), seed=11),
+                                       # one token, and 40 tokens: a single block, mostly padding
+                                       configs.Workload("one_token", B=1, H=2, D=128, F=1, T=1, W=0, ref=0,
+                                                        block_size=16, outlier_heads=(), seed=20),
+                                       configs.Workload("dense_n40", B=1, H=2, D=64, F=5, T=8, W=4, ref=0,
+                                                        block_size=16, outlier_heads=(1,), seed=21)],
                          ids=lambda w: w.name)
 @pytest.mark.parametrize("mode", ["auto", "online"])
 def test_tiles128_one_pass_all_rows(w, mode):
