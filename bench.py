@@ -35,7 +35,13 @@ if ROOT not in sys.path:
 METRIC = "effective TFLOP/s on live blocks, % of GB300 BF16 peak; ms per attention call"
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-LAUNCHES_PER_STEP = 7   # plan meta + plan csr + stats pass1/mean/pass2/finalize + attention
+LAUNCHES_BEFORE_ATTENTION = 6   # plan meta + plan csr + stats pass1/mean/pass2/finalize
+
+
+def attention_launches(plan):
+    """Kernels one attention call launches: the frame-aligned tile pairs (when the
+    plan has any) and the gathered tiles chained to them (when it has any)."""
+    return int(plan.info.n_units > 0) + int(plan.info.n_gathers > 0)
 
 
 def parse_args(argv=None):
@@ -967,10 +973,13 @@ def main(argv=None):
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "traffic": (args.traffic_bytes if args.traffic_bytes is not None
                                      else recorded_traffic(w.name)),
-                         "kernel": f"attn_fwd_kernel<{w.D}>", "peak_source":
+                         "kernel": f"attn_fwd_kernel<{w.D}>" + (
+                             " (tile pairs, and the gathered tiles of "
+                             f"{plan.info.n_gathers} per head chained to them)" if plan.info.n_gathers else ""),
+                         "peak_source":
                          f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
             "block_census": census,
-            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": (LAUNCHES_BEFORE_ATTENTION + attention_launches(plan)) * args.steps,
             "clocks": clocks,
         }
         if e2e:

@@ -56,7 +56,8 @@ class PlanInfo(ctypes.Structure):
                 ("d_row_ptr", ctypes.c_void_p), ("d_col_idx", ctypes.c_void_p),
                 ("d_frame_runs", ctypes.c_void_p), ("d_segments", ctypes.c_void_p),
                 ("d_units", ctypes.c_void_p), ("d_class_off", ctypes.c_void_p),
-                ("part", ctypes.c_int32)]
+                ("part", ctypes.c_int32), ("n_gathers", ctypes.c_int32),
+                ("d_gathers", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -256,6 +257,12 @@ class Plan:
 
     def class_offsets(self):
         return self._device_array(self.info.d_class_off, self.info.n_classes + 1)
+
+    def gathers(self):
+        """Gathered tiles, [n_gathers, 32] int32: pieces, rows, the union of the
+        pieces' key runs (lo0, hi0, lo1, hi1), 1, its key count, then per piece
+        (segment, first row, rows)."""
+        return self._device_array(self.info.d_gathers, 32 * self.info.n_gathers).view(-1, 32)
 
     def close(self):
         if getattr(self, "_h", None) and self._h.value:

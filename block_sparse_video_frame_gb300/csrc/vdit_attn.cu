@@ -34,6 +34,11 @@
 // a pair; the epilogue adds O0 + O1 and the two row sums, exact because both
 // halves share the static bound (online: both halves rescaled to the larger of
 // their two running maxima first).
+// A segment whose rows are not a multiple of 128 leaves a short last tile. The
+// plan packs such tails of several segments into gathered tiles (each row masked
+// to its own key runs); a second instance of this kernel runs them, launched as
+// a programmatic dependent of the first so that its CTAs take the SMs the first
+// one's CTAs leave at its end.
 // Every wait is bounded in time; on expiry the CTA records a site code in the
 // plan's status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -69,6 +74,10 @@ __device__ __forceinline__ void static_for(F &&f) {
         static_for<N, I + 1>(f);
     }
 }
+
+// kernel instances: the frame-aligned tiles of the plan, the frame-blind tiling
+// of the design before frame alignment, the plan's gathered tiles
+enum : int { kModeAligned = 0, kModeTiled = 1, kModeGathered = 2 };
 
 // status-word site codes (which wait expired)
 enum : int {
@@ -123,6 +132,9 @@ struct Params {
     // mask's geometry, which part of it runs, and the 256-row query blocks per head
     int F, T, W, ref, part;
     int n_blocks;
+    // gathered tiles: [n_gathers] records of the plan
+    const int32_t *gathers;
+    int n_gathers;
 };
 
 struct Work {
@@ -134,6 +146,7 @@ struct Work {
     int nt0, nkt;          // key tiles of run 0, total key tiles
     bool stat;             // static-max softmax (else online)
     bool alt;              // lone static tile: slots 0 and 1 take alternate key tiles
+    int gat;               // gathered tile: its record
 };
 
 // Work order. CTA b takes work items b, b + grid, b + 2*grid, ... The items walk
@@ -235,9 +248,50 @@ __device__ __forceinline__ void decode_tiled(const Params &p, long long w, Work 
     u.alt = u.nact == 1 && u.nkt >= 2;
 }
 
-template <bool kTiled>
+// Gathered tiles (the second launch): item w is record w % n_gathers of head
+// w / n_gathers. One query tile, whose rows come from up to 8 segments, over the
+// union of their key runs; with per-segment bounds it takes the static path only
+// if every piece's segment may.
+__device__ __forceinline__ void decode_gathered(const Params &p, long long w, Work &u) {
+    u.bh = (int)(w / p.n_gathers);
+    u.gat = (int)(w % p.n_gathers);
+    u.b = u.bh / p.H;
+    u.h = u.bh % p.H;
+    const int32_t *g = p.gathers + kGatherInts * u.gat;
+    u.seg = -1;
+    u.pair = 0;
+    u.row0 = 0; u.rows = g[1];
+    u.lo0 = g[2]; u.hi0 = g[3]; u.lo1 = g[4]; u.hi1 = g[5];
+    u.ntile = 1;
+    u.nact = 1;
+    u.nt0 = (u.hi0 - u.lo0 + kBK - 1) / kBK;
+    u.nkt = u.nt0 + (u.hi1 - u.lo1 + kBK - 1) / kBK;
+    // the eligibility arrays are read in AUTO mode only (they may be null otherwise)
+    bool elig = p.mode == VDIT_MODE_AUTO;
+    if (elig && !p.seg_elig) elig = p.elig[u.bh] != 0;
+    for (int k = 0; elig && p.seg_elig && k < g[0]; ++k)
+        elig = p.seg_elig[(size_t)u.bh * p.nseg + g[kGatherPiece + 3 * k]] != 0;
+    u.stat = p.mode == VDIT_MODE_FORCE_STATIC || elig;
+    u.alt = u.nkt >= 2;
+}
+
+// Row r of gathered tile `gat`: its sequence row, and in seg its segment. Rows
+// past the last piece repeat that piece's rows (computed, never stored).
+__device__ __forceinline__ int gathered_row(const Params &p, int gat, int r, int &seg) {
+    const int32_t *g = p.gathers + kGatherInts * gat;
+    int k = 0, off = 0;
+    while (k < g[0] - 1 && r >= off + g[kGatherPiece + 3 * k + 2]) {
+        off += g[kGatherPiece + 3 * k + 2];
+        ++k;
+    }
+    seg = g[kGatherPiece + 3 * k];
+    return g[kGatherPiece + 3 * k + 1] + (r - off) % g[kGatherPiece + 3 * k + 2];
+}
+
+template <int kMode>
 __device__ __forceinline__ void decode_any(const Params &p, long long w, Work &u) {
-    if constexpr (kTiled) decode_tiled(p, w, u);
+    if constexpr (kMode == kModeTiled) decode_tiled(p, w, u);
+    else if constexpr (kMode == kModeGathered) decode_gathered(p, w, u);
     else decode(p, w, u);
 }
 
@@ -282,10 +336,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-template <int D, bool kTiled>
+// tm_q: 128-row boxes; in the gathered instance 16-row boxes (pieces are
+// multiples of 16 rows)
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    constexpr bool kTiled = kMode == kModeTiled;
+    constexpr bool kGathered = kMode == kModeGathered;
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -335,6 +393,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the gathered-tile launch that follows may place its CTAs as SMs free up
+    if constexpr (kMode == kModeAligned) grid_launch_dependents();
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
@@ -343,16 +403,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x) {
                 Work u;
-                decode_any<kTiled>(p, w, u);
+                decode_any<kMode>(p, w, u);
                 if (kTiled && u.nkt == 0) continue;   // a block with no live key: no work
                 if (!(ok = mbar_wait(bar(kBarQfree), (it & 1) ^ 1, abort_flag, p.status, kSiteQfree, tlim)))
                     break;
                 mbar_arrive_expect_tx(bar(kBarQfull), (uint32_t)(u.nact * L::kTileBytes));
-                for (int q = 0; q < u.nact; ++q) {
-                    const int row = tile_row(u, q);
-                    for (int hf = 0; hf < D / 64; ++hf)
-                        tma_load_4d(sbase + L::kQ + q * L::kTileBytes + hf * kHalfBytes, &tm_q,
-                                    bar(kBarQfull), hf * 64, row, u.h, u.b);
+                if constexpr (kGathered) {
+                    // 16-row groups from the tile's pieces
+                    for (int r0 = 0; r0 < kTileRows; r0 += 16) {
+                        int sg;
+                        const int row = gathered_row(p, u.gat, r0, sg);
+                        for (int hf = 0; hf < D / 64; ++hf)
+                            tma_load_4d(sbase + L::kQ + hf * kHalfBytes + r0 * 128, &tm_q, bar(kBarQfull),
+                                        hf * 64, row, u.h, u.b);
+                    }
+                } else {
+                    for (int q = 0; q < u.nact; ++q) {
+                        const int row = tile_row(u, q);
+                        for (int hf = 0; hf < D / 64; ++hf)
+                            tma_load_4d(sbase + L::kQ + q * L::kTileBytes + hf * kHalfBytes, &tm_q,
+                                        bar(kBarQfull), hf * 64, row, u.h, u.b);
+                    }
                 }
                 ++it;
                 for (int j = 0; j < u.nkt; ++j) {
@@ -433,7 +504,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
-            decode_any<kTiled>(p, w, u);
+            decode_any<kMode>(p, w, u);
             if (kTiled && u.nkt == 0) { --it; continue; }   // skipped by every role: no phase used
             if (!(ok = wait(kBarQfull, it & 1, kSiteQfullMma))) break;
             const uint32_t kc0 = kc;
@@ -554,7 +625,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < p.total_work; w += gridDim.x, ++it) {
             Work u;
-            decode_any<kTiled>(p, w, u);
+            decode_any<kMode>(p, w, u);
             if (kTiled && u.nkt == 0) {
                 // skipped by every role (no phase used): a block none of whose rows
                 // sees a key of this part of the mask stores O = 0 and LSE = -inf
@@ -589,6 +660,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const bool stat = u.stat;
             ok = mbar_wait_warp(bar(kBarQfull), it & 1, abort_flag, p.status, kSiteQfullSm, tlim);
             if (!ok) break;
+            // a gathered tile's row: its segment (the bound's R, the row's key runs)
+            int gseg = u.seg;
+            if constexpr (kGathered) gathered_row(p, u.gat, r, gseg);
             // row bound ("Unchaining the Softmax"): m~ = scale*log2e*(q.c + |q| R)
             float mt = 0.f;
             if (act && stat) {
@@ -614,7 +688,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     }
                 }
-                const float R = p.seg_rmax ? p.seg_rmax[(size_t)u.bh * p.nseg + u.seg] : p.k_rmax[u.bh];
+                const float R = p.seg_rmax ? p.seg_rmax[(size_t)u.bh * p.nseg + gseg] : p.k_rmax[u.bh];
                 mt = sc * (dot + sqrtf(nn) * R);
             }
             __syncwarp();
@@ -623,8 +697,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
             float l0 = 0.f, l1 = 0.f, mrun = -INFINITY;
             const int j0 = u.alt ? q : 0;          // this warpgroup's first key tile
-            int rlo0 = 0, rhi0 = 0, rlo1 = 0, rhi1 = 0;   // frame-blind tiling: this row's live keys
+            int rlo0 = 0, rhi0 = 0, rlo1 = 0, rhi1 = 0;   // this row's live keys
             if constexpr (kTiled) row_runs(p, tile_row(u, u.alt ? 0 : q) + r, rlo0, rhi0, rlo1, rhi1);
+            if constexpr (kGathered) {
+                const int32_t *sg = p.segments + kSegInts * gseg;
+                rlo0 = sg[2]; rhi0 = sg[3]; rlo1 = sg[4]; rhi1 = sg[5];
+            }
             for (int j = j0; j < u.nkt; j += u.alt ? 2 : 1) {
                 int start, nvalid;
                 key_tile(u, j, start, nvalid);
@@ -682,12 +760,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     l1 += a1;
                 };
                 // frame-blind tiling: in a tile that straddles a frame boundary the mask
-                // predicate, per element, turns this row's dead keys (and padding) into -inf
-                auto mask = [&](uint32_t (&v)[128]) {
-                    if constexpr (kTiled) {
-                        const bool full = (rlo0 <= start && start + kBK <= rhi0) ||
-                                          (rlo1 <= start && start + kBK <= rhi1);
-                        if (!__all_sync(0xffffffffu, full)) {
+                // predicate, per element, turns this row's dead keys (and padding) into
+                // -inf. Gathered tiles mask each row to its own key runs; there a row
+                // that sees no key of the tile returns true and takes an infinite shift
+                // (p = 0) instead, unless the warp masks per element anyway because one
+                // of its rows straddles a run boundary.
+                auto mask = [&](uint32_t (&v)[128]) -> bool {
+                    if constexpr (kTiled || kGathered) {
+                        const int kend = start + (kTiled ? kBK : nvalid);
+                        const bool full = (rlo0 <= start && kend <= rhi0) || (rlo1 <= start && kend <= rhi1);
+                        const bool dead = kGathered && !(rlo0 < kend && start < rhi0) && !(rlo1 < kend && start < rhi1);
+                        if (!__all_sync(0xffffffffu, full || dead)) {
 #pragma unroll
                             for (int e = 0; e < 128; ++e) {
                                 const int jk = start + e;
@@ -695,8 +778,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                                   (unsigned)(jk - rlo1) < (unsigned)(rhi1 - rlo1);
                                 v[e] = live ? v[e] : 0xff800000u;
                             }
+                            return false;
                         }
+                        return dead;
                     }
+                    return false;
                 };
                 // Each path loads the whole S row in one TMEM load of its own: a load
                 // shared by both paths ahead of the branch measured 8% slower on the
@@ -704,12 +790,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (stat) {
                     uint32_t v[128];
                     tmem_ld128(tS, v);
-                    mask(v);
-                    exps(v, mt);
+                    const bool dead = mask(v);
+                    exps(v, dead ? INFINITY : mt);
                 } else {
                     uint32_t v[128];
                     tmem_ld128(tS, v);
-                    mask(v);
+                    const bool dead = mask(v);
                     // online: this tile's row max, taken on the raw logits (the scale is
                     // positive), then the lazy rescale decision
                     float mx;
@@ -726,7 +812,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 128; ++e) mx = e < nvalid ? fmaxf(mx, __uint_as_float(v[e])) : mx;
                     }
-                    mx *= sc;
+                    mx = dead ? -INFINITY : mx * sc;
                     float alpha = 1.f;      // factor of the O rescale (lazy, warp-uniform)
                     bool rescale = false;
                     if (j == j0) {
@@ -741,9 +827,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             if (need) mrun = mx;
                         }
                     }
-                    // no live key in this row yet (frame-blind tiling): every term is
-                    // masked, any finite shift gives p = 0
-                    exps(v, kTiled && mrun == -INFINITY ? 0.f : mrun);
+                    // no live key in this row yet (frame-blind tiling, gathered tile):
+                    // every term is masked, any finite shift gives p = 0
+                    exps(v, dead ? INFINITY : (kTiled || kGathered) && mrun == -INFINITY ? 0.f : mrun);
                     if (rescale) {
                         // O (after P.V of the previous key tile, which the S barrier of
                         // this tile covers) scaled to the new running max, before this
@@ -820,10 +906,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // mask under the frame-blind tiling) stores O = 0 and LSE = -inf
             const float inv = kTiled && l == 0.f ? 0.f : 1.0f / l;
             const int t = kTilesPerUnit * u.pair + q;
-            const int row = tile_row(u, q) + r;
+            const int row = kGathered ? gathered_row(p, u.gat, r, gseg) : tile_row(u, q) + r;
             const int own_lo = u.row0 + t * kTileRows;
             const int own_hi = u.row0 + min((t + 1) * kTileRows, u.rows);
-            const bool owned = row >= own_lo && row < own_hi && (!kTiled || row < p.N);
+            const bool owned = kGathered ? r < u.rows : row >= own_lo && row < own_hi && (!kTiled || row < p.N);
             const long long obase = (long long)u.b * p.os0 + (long long)u.h * p.os1 + (long long)row * p.os2;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -884,6 +970,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // the gathered launch completes only after the launch it depends on, so work
+    // the stream orders after it also follows that launch
+    if constexpr (kGathered) grid_dependency_wait();
 }
 
 // ---------------------------------------------------------------- host side
@@ -906,13 +995,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B, H, N, D] bf16 tensor -> 4-D tensor map with a 64 x 128 x 1 x 1 box, 128-byte swizzle.
-bool encode_bhnd(CUtensorMap *m, const void *base, int B, int H, int N, int D, const int64_t st[3]) {
+// [B, H, N, D] bf16 tensor -> 4-D tensor map with a 64 x rows x 1 x 1 box, 128-byte swizzle.
+bool encode_bhnd(CUtensorMap *m, const void *base, int B, int H, int N, int D, const int64_t st[3],
+                 unsigned rows = 128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t box[4] = {64, rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -928,13 +1018,13 @@ static_assert(Layout<64>::kBytes <= Layout<64>::kAlloc && Layout<64>::kAlloc <= 
               "the D = 64 layout must fit the shared-memory request");
 static_assert(kSmemRequest <= 227 * 1024, "shared memory beyond the per-CTA limit");
 
-template <int D, bool kTiled>
+template <int D, int kMode>
 cudaError_t prepare_kernel(int device) {
     static std::mutex mu;
     static bool done[64] = {};
     std::lock_guard<std::mutex> g(mu);
     if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kTiled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemRequest);
     if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
     return e;
@@ -1066,9 +1156,11 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
         return VDIT_ERR_INVALID;
     }
     const int N = (int)plan->N;
-    CUtensorMap tq, tk, tv;
+    // the gathered tiles (second launch) read Q in 16-row boxes
+    const bool gathered = !tiled && plan->h.n_gathers > 0;
+    CUtensorMap tq, tk, tv, tq16;
     if (!encode_bhnd(&tq, q, B, H, N, D, q_strides) || !encode_bhnd(&tk, k, B, H, N, D, k_strides) ||
-        !encode_bhnd(&tv, v, B, H, N, D, v_strides)) {
+        !encode_bhnd(&tv, v, B, H, N, D, v_strides) || (gathered && !encode_bhnd(&tq16, q, B, H, N, D, q_strides, 16))) {
         set_error("vdit_attn_fwd: cuTensorMapEncodeTiled failed (alignment/strides or driver entry point)");
         return VDIT_ERR_INVALID;
     }
@@ -1091,30 +1183,59 @@ vdit_status attn_fwd_impl(const vdit_plan *plan, const void *q, const void *k, c
     prm.timeout_ns = wait_limit_ns();
     prm.F = plan->F; prm.T = plan->T; prm.W = plan->W; prm.ref = plan->ref; prm.part = plan->part;
     prm.n_blocks = (int)((N + kTilesPerUnit * kTileRows - 1) / (kTilesPerUnit * kTileRows));
+    prm.gathers = plan->d_gathers;
+    prm.n_gathers = plan->h.n_gathers;
     if (tiled) prm.total_work = (long long)B * H * prm.n_blocks;
     const int nsm = sm_count(dev);
     if (nsm <= 0) { set_error("vdit_attn_fwd: cannot query SM count"); return VDIT_ERR_CUDA; }
     const long long grid = prm.total_work < nsm ? prm.total_work : nsm;
-    if (grid <= 0) return VDIT_OK;
+    const long long gwork = gathered ? (long long)B * H * plan->h.n_gathers : 0;
+    if (grid <= 0 && gwork <= 0) return VDIT_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_fails_by_hook()) {
         set_error("vdit_attn_fwd: launch failure injected by vdit_set_launch_fail_after");
         return VDIT_ERR_CUDA;
     }
-    if (D == 128 && !tiled) {
-        VDIT_CUDA_TRY((prepare_kernel<128, false>(dev)));
-        attn_fwd_kernel<128, false><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
-    } else if (D == 64 && !tiled) {
-        VDIT_CUDA_TRY((prepare_kernel<64, false>(dev)));
-        attn_fwd_kernel<64, false><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
-    } else if (D == 128) {
-        VDIT_CUDA_TRY((prepare_kernel<128, true>(dev)));
-        attn_fwd_kernel<128, true><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
-    } else {
-        VDIT_CUDA_TRY((prepare_kernel<64, true>(dev)));
-        attn_fwd_kernel<64, true><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+    if (grid > 0) {
+        if (D == 128 && !tiled) {
+            VDIT_CUDA_TRY((prepare_kernel<128, kModeAligned>(dev)));
+            attn_fwd_kernel<128, kModeAligned><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+        } else if (D == 64 && !tiled) {
+            VDIT_CUDA_TRY((prepare_kernel<64, kModeAligned>(dev)));
+            attn_fwd_kernel<64, kModeAligned><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+        } else if (D == 128) {
+            VDIT_CUDA_TRY((prepare_kernel<128, kModeTiled>(dev)));
+            attn_fwd_kernel<128, kModeTiled><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+        } else {
+            VDIT_CUDA_TRY((prepare_kernel<64, kModeTiled>(dev)));
+            attn_fwd_kernel<64, kModeTiled><<<(unsigned)grid, kThreads, kSmemRequest, s>>>(tq, tk, tv, prm);
+        }
+        VDIT_CUDA_TRY(cudaGetLastError());
     }
-    VDIT_CUDA_TRY(cudaGetLastError());
+    if (gwork > 0) {
+        // the gathered tiles: a programmatic dependent of the launch above (which
+        // lets it place CTAs once every CTA of that launch runs), so its CTAs take
+        // the SMs that launch leaves at its end
+        Params pg = prm;
+        pg.total_work = gwork;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(gwork < nsm ? gwork : nsm));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemRequest;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = grid > 0 ? 1 : 0;
+        if (D == 128) {
+            VDIT_CUDA_TRY((prepare_kernel<128, kModeGathered>(dev)));
+            VDIT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_kernel<128, kModeGathered>, tq16, tk, tv, pg));
+        } else {
+            VDIT_CUDA_TRY((prepare_kernel<64, kModeGathered>(dev)));
+            VDIT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_fwd_kernel<64, kModeGathered>, tq16, tk, tv, pg));
+        }
+    }
     return VDIT_OK;
 }
 

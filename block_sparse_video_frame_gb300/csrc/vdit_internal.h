@@ -44,6 +44,13 @@ constexpr int kSegInts = 8;      // ints per segment record
 constexpr int kMaxFrames = 4096; // frames a plan may hold
 constexpr int kMaxClasses = 64;  // distinct unit costs a plan may hold
 constexpr int kMaxPairsPerSegment = 1 << 16;  // tile pairs a segment may hold (16-bit field)
+// Gathered tiles: the ragged last rows of several segments (each a multiple of
+// 16 rows, at most kGatherMaxRows) share one 128-row query tile. A record holds
+// its piece count, rows, the union of the pieces' key runs and the pieces.
+constexpr int kGatherMaxPieces = 8;
+constexpr int kGatherMaxRows = 64;
+constexpr int kGatherPiece = 8;                                  // first piece: seg, row0, rows
+constexpr int kGatherInts = kGatherPiece + 3 * kGatherMaxPieces; // ints per gathered-tile record
 
 // A scale factor the kernels can use: positive and finite (NaN and +inf fail).
 inline bool finite_positive(float x) { return x > 0.f && x <= 3.402823466e38f; }
@@ -56,6 +63,7 @@ struct PlanHeader {
     int n_units;
     int n_classes;
     int error; // non-zero: the kernel found an inconsistent request
+    int n_gathers;
 };
 
 }  // namespace vdit
@@ -75,6 +83,7 @@ struct vdit_plan {
     int32_t *d_segments = nullptr;
     int32_t *d_units = nullptr;
     int32_t *d_class_off = nullptr;
+    int32_t *d_gathers = nullptr;
     int32_t *d_status = nullptr;
     int units_cap = 0;
 };

@@ -71,18 +71,48 @@ __device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_fram
     r[0] = lo0; r[1] = hi0; r[2] = lo1; r[3] = hi1;
 }
 
+// Union of a gathered tile's key runs r (empty runs have hi <= lo) with a
+// segment's runs s, written to u as at most two ascending runs; false when the
+// union needs more than two.
+__device__ bool union_runs(const int r[4], const int32_t *s, int u[4]) {
+    int lo[4], hi[4], n = 0;
+    for (int i = 0; i < 2; ++i) {
+        if (r[2 * i + 1] > r[2 * i]) { lo[n] = r[2 * i]; hi[n] = r[2 * i + 1]; ++n; }
+        if (s[2 * i + 1] > s[2 * i]) { lo[n] = s[2 * i]; hi[n] = s[2 * i + 1]; ++n; }
+    }
+    for (int i = 1; i < n; ++i)
+        for (int j = i; j > 0 && lo[j - 1] > lo[j]; --j) {
+            const int tl = lo[j], th = hi[j];
+            lo[j] = lo[j - 1]; hi[j] = hi[j - 1];
+            lo[j - 1] = tl; hi[j - 1] = th;
+        }
+    int m = 0;
+    for (int i = 0; i < n; ++i) {
+        if (m > 0 && lo[i] <= hi[m - 1]) {
+            hi[m - 1] = max(hi[m - 1], hi[i]);
+        } else {
+            lo[m] = lo[i]; hi[m] = hi[i]; ++m;
+        }
+    }
+    if (m > 2) return false;
+    u[0] = m > 0 ? lo[0] : 0; u[1] = m > 0 ? hi[0] : 0;
+    u[2] = m > 1 ? lo[1] : 0; u[3] = m > 1 ? hi[1] : 0;
+    return true;
+}
+
 // One block. The frames' runs are computed in parallel; one thread then builds
-// the segments, sorts them and lays out the cost classes, with every
-// intermediate in shared memory (the runs of a frame are recomputed, not read
-// back); the unit list is written by all threads.
+// the segments, packs their ragged last rows into gathered tiles, sorts the
+// segments and lays out the cost classes, with every intermediate in shared
+// memory (the runs of a frame are recomputed, not read back); the unit list is
+// written by all threads.
 __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32_t *__restrict__ frame_runs,
                                  int32_t *__restrict__ segments, int32_t *__restrict__ units,
-                                 int32_t *__restrict__ class_off) {
+                                 int32_t *__restrict__ class_off, int32_t *__restrict__ gathers) {
     // s_cnt: live frames per frame, then per segment its key count, then its first unit.
     // s_order: segments longest first, each entry (tile pairs << 12) | segment.
     __shared__ int s_cnt[kMaxFrames];
     __shared__ int s_order[kMaxFrames];
-    __shared__ int s_nused;   // segments that get units (in s_order)
+    __shared__ int s_nused;   // entries of s_order that get units
     static_assert(kMaxFrames <= (1 << 12), "segment index field of s_order");
     for (int f = threadIdx.x; f < a.F; f += blockDim.x) {
         int r[4], live;
@@ -112,14 +142,12 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             int32_t *g = segments + kSegInts * nseg;
             const int ntile = (rows + kTileRows - 1) / kTileRows;
             const int keys = (cur[1] - cur[0]) + (cur[3] - cur[2]);
-            const int npairs = (ntile + kTilesPerUnit - 1) / kTilesPerUnit;
             g[0] = row0; g[1] = rows;
             g[2] = cur[0]; g[3] = cur[1]; g[4] = cur[2]; g[5] = cur[3];
             g[6] = ntile; g[7] = keys;
             // a unit code keeps the tile pair in its low 16 bits
-            if (npairs > kMaxPairsPerSegment) h.error = 4;
+            if ((ntile + kTilesPerUnit - 1) / kTilesPerUnit > kMaxPairsPerSegment) h.error = 4;
             s_cnt[nseg] = keys;        // frame counts are no longer needed
-            s_order[nseg] = (min(npairs, kMaxPairsPerSegment) << 12) | nseg;
             ++nseg;
         };
         for (int f = 0; f < a.F; ++f) {
@@ -136,6 +164,58 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
         }
         flush();
         if (h.error != 0) nseg = 0;
+        // gathered tiles -----------------------------------------------------
+        // A segment whose row count is not a multiple of 128 ends in a tile that
+        // holds only its last rows % 128 rows. Consecutive such tails (multiples
+        // of 16 rows, at most kGatherMaxRows each) are packed into one 128-row
+        // tile that visits the union of their key runs, when that union is at
+        // most two runs and at least a quarter smaller than the key runs the
+        // tails would each visit in a tile of their own; the segments then keep
+        // only their whole tiles. The gathered tiles are not work units: a second
+        // launch of the attention kernel runs them.
+        int ng = 0;
+        {
+            int np = 0, grows = 0, gr[4] = {0, 0, 0, 0};
+            long long sum_keys = 0;
+            auto close = [&]() {
+                int32_t *rec = gathers + kGatherInts * ng;
+                const long long ukeys = (long long)(gr[1] - gr[0]) + (gr[3] - gr[2]);
+                if (np >= 2 && 4 * ukeys <= 3 * sum_keys) {
+                    rec[0] = np; rec[1] = grows;
+                    rec[2] = gr[0]; rec[3] = gr[1]; rec[4] = gr[2]; rec[5] = gr[3];
+                    rec[6] = 1; rec[7] = (int)ukeys;
+                    for (int k = 0; k < np; ++k) {
+                        int32_t *g = segments + kSegInts * rec[kGatherPiece + 3 * k];
+                        g[6] = g[1] / kTileRows;
+                    }
+                    ++ng;
+                }
+                np = 0; grows = 0; sum_keys = 0;
+                gr[0] = gr[1] = gr[2] = gr[3] = 0;
+            };
+            for (int sg = 0; sg < nseg; ++sg) {
+                const int32_t *g = segments + kSegInts * sg;
+                const int tail = g[1] % kTileRows;
+                if (g[7] == 0 || tail == 0 || tail % 16 != 0 || tail > kGatherMaxRows) continue;
+                int u[4];
+                const bool joins = union_runs(gr, g + 2, u) && np < kGatherMaxPieces && grows + tail <= kTileRows;
+                if (np > 0 && !joins) {
+                    close();
+                    union_runs(gr, g + 2, u);
+                }
+                int32_t *pc = gathers + kGatherInts * ng + kGatherPiece + 3 * np;
+                pc[0] = sg; pc[1] = g[0] + g[1] - tail; pc[2] = tail;
+                gr[0] = u[0]; gr[1] = u[1]; gr[2] = u[2]; gr[3] = u[3];
+                grows += tail;
+                sum_keys += g[7];
+                ++np;
+            }
+            close();
+        }
+        for (int i = 0; i < nseg; ++i) {
+            const int npairs = (segments[kSegInts * i + 6] + kTilesPerUnit - 1) / kTilesPerUnit;
+            s_order[i] = (min(npairs, kMaxPairsPerSegment) << 12) | i;
+        }
         // longest first (stable insertion sort on key count) ------------------
         for (int i = 1; i < nseg; ++i) {
             const int v = s_order[i], key = s_cnt[v & 0xFFF];
@@ -147,10 +227,11 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             s_order[j + 1] = v;
         }
         // cost classes and the first unit of each segment ---------------------
-        int nu = 0, ncls = 0, prev_key = -1, used = 0;
-        for (int i = 0; i < nseg; ++i) {
+        int nu = 0, ncls = 0, prev_key = -1, i = 0;
+        for (; i < nseg; ++i) {
             const int v = s_order[i], sg = v & 0xFFF, np = v >> 12, key = s_cnt[sg];
             if (key == 0) break;   // frames that see no key (reference part only): no work, sorted last
+            if (np == 0) continue; // every row of the segment went to gathered tiles
             if (key != prev_key) {
                 if (ncls >= kMaxClasses) { h.error = 2; break; }
                 class_off[ncls++] = nu;
@@ -159,14 +240,14 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             if (nu + np > a.units_cap) { h.error = 3; break; }
             s_cnt[sg] = nu;
             nu += np;
-            ++used;
         }
         class_off[ncls] = nu;
         h.n_segments = nseg;
         h.n_units = nu;
         h.n_classes = ncls;
+        h.n_gathers = ng;
         *hdr = h;
-        s_nused = used;
+        s_nused = i;
     }
     __syncthreads();
     // units: (segment << 16) | tile pair, in the order of s_order ------------
@@ -263,6 +344,7 @@ void free_plan_buffers(vdit_plan *p) {
     cudaFree(p->d_segments);
     cudaFree(p->d_units);
     cudaFree(p->d_class_off);
+    cudaFree(p->d_gathers);
     cudaFree(p->d_status);
 }
 
@@ -271,7 +353,7 @@ void free_plan_buffers(vdit_plan *p) {
 cudaError_t launch_plan_kernels(const vdit_plan *p, cudaStream_t stream, bool csr) {
     PlanArgs a = args_of(p);
     plan_meta_kernel<<<1, 256, 0, stream>>>(a, p->d_header, p->d_frame_runs, p->d_segments,
-                                             p->d_units, p->d_class_off);
+                                             p->d_units, p->d_class_off, p->d_gathers);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !csr) return e;
     plan_csr_kernel<<<(a.nqb + 7) / 8, 256, 0, stream>>>(a, p->d_frame_runs, p->d_row_ptr, p->d_col_idx);
@@ -336,6 +418,8 @@ vdit_status plan_create(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_segments), sizeof(int32_t) * kSegInts * F);
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_units), sizeof(int32_t) * p->units_cap);
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_class_off), sizeof(int32_t) * (kMaxClasses + 1));
+    // a gathered tile holds at least two segments' rows
+    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_gathers), sizeof(int32_t) * kGatherInts * (F / 2 + 1));
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_status), sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) {
@@ -422,6 +506,8 @@ extern "C" vdit_status vdit_plan_get_info(const vdit_plan *p, vdit_plan_info *in
     info->n_units = p->h.n_units;
     info->n_classes = p->h.n_classes;
     info->part = p->part;
+    info->n_gathers = p->h.n_gathers;
+    info->d_gathers = p->d_gathers;
     info->d_row_ptr = p->d_row_ptr;
     info->d_col_idx = p->d_col_idx;
     info->d_frame_runs = p->d_frame_runs;

@@ -80,10 +80,20 @@ typedef struct {
     const int32_t *d_row_ptr;    /* [n_qblocks + 1] CSR row offsets */
     const int32_t *d_col_idx;    /* [nnz] live key blocks, ascending per row */
     const int32_t *d_frame_runs; /* [F][4]: lo0, hi0, lo1, hi1 key tokens; (0,0) = no 2nd run */
-    const int32_t *d_segments;   /* [n_segments][8]: row0, rows, lo0, hi0, lo1, hi1, ntiles, keys */
+    const int32_t *d_segments;   /* [n_segments][8]: row0, rows, lo0, hi0, lo1, hi1, ntiles, keys;
+                                    ntiles = ceil(rows / 128), or floor when the segment's
+                                    last rows % 128 rows went to a gathered tile */
     const int32_t *d_units;      /* [n_units]: (segment << 16) | tile pair, longest first */
     const int32_t *d_class_off;  /* [n_classes + 1] unit offsets of the cost classes */
     int32_t part;                /* VDIT_PART_*: the part of the mask this plan schedules */
+    int32_t n_gathers;           /* gathered tiles per head: 128-row query tiles that hold
+                                    the ragged last rows (rows % 128, a multiple of 16 up to
+                                    64) of two to eight segments and visit the union of their
+                                    key runs (at most two runs, at least a quarter fewer keys
+                                    than the tails would visit apart), masking each row to
+                                    its own runs; vdit_attn_fwd runs them in a second launch */
+    const int32_t *d_gathers;    /* [n_gathers][32]: pieces, rows, lo0, hi0, lo1, hi1 (the
+                                    union), 1, keys, then per piece: segment, first row, rows */
 } vdit_plan_info;
 
 /* Build the block schedule of the frame-window + reference-frame mask

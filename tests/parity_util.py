@@ -14,10 +14,11 @@ LSE_ABS = 1e-3
 
 def stratified_rows(w, per_frame_random=13, seed=1234):
     """Flattened row indices ((b*H + h)*N + i): per (b, h, frame) the frame's
-    first and last row and `per_frame_random` seeded uniform rows; per segment
-    (rows sharing one key-run list: a frame, or the whole sequence when dense)
-    the first row of its last 128-row tile, which is shifted to end at the
-    segment's end."""
+    first and last row, the first row of its last T % 128 rows and the row
+    before it (a tail that a gathered tile may hold, and the last whole tile),
+    and `per_frame_random` seeded uniform rows; per segment (rows sharing one
+    key-run list: a frame, or the whole sequence when dense) the first row of
+    its last 128-row tile, which is shifted to end at the segment's end."""
     rng = np.random.default_rng(seed)
     rows = []
     seg = w.N if w.dense else w.T
@@ -26,6 +27,8 @@ def stratified_rows(w, per_frame_random=13, seed=1234):
         for f in range(w.F):
             lo, hi = f * w.T, (f + 1) * w.T
             picks.update((lo, hi - 1))
+            if w.T % 128 and w.T > 128:
+                picks.update((hi - w.T % 128, hi - w.T % 128 - 1))
             picks.update(int(x) for x in rng.integers(lo, hi, per_frame_random))
         for s0 in range(0, w.N, seg):
             picks.add(max(s0, s0 + seg - 128))

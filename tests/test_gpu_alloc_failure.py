@@ -11,7 +11,8 @@ from block_sparse_video_frame_gb300 import configs
 
 pytestmark = pytest.mark.gpu
 
-PLAN_ALLOCATIONS = 8   # header, frame runs, segments, units, class offsets, status, row_ptr, col_idx
+PLAN_ALLOCATIONS = 9   # header, frame runs, segments, units, class offsets, gathered tiles, status,
+                       # row_ptr, col_idx
 
 
 def make_plan(w):

@@ -38,36 +38,85 @@ def test_schedule_bit_exact(F, T, W, ref, bs):
 
 
 @pytest.mark.parametrize("F,T,W,ref,bs", CASES)
-def test_work_units_cover_every_query_tile_once(F, T, W, ref, bs):
-    """Host-logic check of the attention work list: every 128-row query tile of
-    every segment appears in exactly one unit; segments group frames with equal
-    key runs; units are ordered by non-increasing key count."""
+def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
+    """Host-logic check of the attention work list: every query row is owned by
+    exactly one 128-row tile, either a tile of its segment or a gathered tile;
+    segments group frames with equal key runs; a gathered tile holds the ragged
+    last rows of 2 to 8 segments (multiples of 16, at most 64 each, 128 in all)
+    and visits the union of their key runs, at least a quarter smaller than the
+    runs the tails would each visit alone; the units (tile pairs of segments
+    that see keys) are ordered by non-increasing key count, one count per cost
+    class."""
     plan = vd.attn_plan(F, T, W, ref, bs)
     runs = plan.frame_runs().cpu().numpy()
     segs = plan.segments().cpu().numpy()
     units = plan.units().cpu().numpy()
     cls = plan.class_offsets().cpu().numpy()
+    gat = plan.gathers().cpu().numpy()
     N = F * T
     covered = np.zeros(N, dtype=np.int64)
-    for s in segs:
-        row0, rows, lo0, hi0, lo1, hi1, ntile, keys = s
+    gathered_seg = set()
+    for gi, g in enumerate(gat):
+        npc, rows, lo0, hi0, lo1, hi1, one, keys = (int(x) for x in g[:8])
+        assert 2 <= npc <= 8 and one == 1 and 0 < rows <= 128
+        assert keys == (hi0 - lo0) + (hi1 - lo1) and lo0 < hi0 and (hi1 == lo1 == 0 or hi0 < lo1 < hi1)
+        live = np.zeros(N, dtype=bool)
+        live[lo0:hi0] = True
+        live[lo1:hi1] = True
+        total, sum_keys = 0, 0
+        for k in range(npc):
+            sg, r0, nr = (int(x) for x in g[8 + 3 * k:11 + 3 * k])
+            s = segs[sg]
+            assert nr == s[1] % 128 and nr % 16 == 0 and nr <= 64 and r0 == s[0] + s[1] - nr
+            assert live[s[2]:s[3]].all() and live[s[4]:s[5]].all()
+            covered[r0:r0 + nr] += 1
+            total += nr
+            sum_keys += int(s[7])
+            gathered_seg.add(sg)
+        assert total == rows and 4 * keys <= 3 * sum_keys
+    for si, s in enumerate(segs):
+        row0, rows, lo0, hi0, lo1, hi1, ntile, keys = (int(x) for x in s)
         f0 = row0 // T
         for f in range(f0, f0 + rows // T):
             assert list(runs[f]) == [lo0, hi0, lo1, hi1]
-        assert ntile == (rows + 127) // 128 and keys == (hi0 - lo0) + (hi1 - lo1)
-        covered[row0:row0 + rows] += 1
+        assert keys == (hi0 - lo0) + (hi1 - lo1)
+        if si in gathered_seg:
+            assert ntile == rows // 128
+            covered[row0:row0 + ntile * 128] += 1
+        else:
+            assert ntile == (rows + 127) // 128
+            covered[row0:row0 + rows] += 1
     assert (covered == 1).all()
     seen = {}
     for code in units:
-        seg, pair = int(code) >> 16, int(code) & 0xFFFF
-        seen[(seg, pair)] = seen.get((seg, pair), 0) + 1
-    want = {(si, p) for si, s in enumerate(segs) for p in range((s[6] + 1) // 2)}
+        idx, pair = int(code) >> 16, int(code) & 0xFFFF
+        seen[(idx, pair)] = seen.get((idx, pair), 0) + 1
+    want = {(si, p) for si, s in enumerate(segs) if s[7] > 0 for p in range((s[6] + 1) // 2)}
     assert set(seen) == want and all(c == 1 for c in seen.values())
     keys = np.array([segs[int(c) >> 16][7] for c in units])
     assert (np.diff(keys) <= 0).all()
     assert cls[0] == 0 and cls[-1] == len(units)
     for a, b in zip(cls[:-1], cls[1:]):
         assert len(set(keys[a:b])) == 1
+
+
+def test_gathered_tiles_of_the_720p_geometry():
+    """13 frames of 3600 tokens (28 whole tiles and a 16-row tail each), window
+    +-2 and reference frame 0: the tails of frames 0-7 share one tile over frames
+    0-9, those of frames 8-12 one over frames 6-12 plus frame 0; every segment
+    keeps 28 tiles."""
+    T = 3600
+    plan = vd.attn_plan(13, T, 2, 0, 240)
+    segs = plan.segments().cpu().numpy()
+    gat = plan.gathers().cpu().numpy()
+    assert len(segs) == 13 and (segs[:, 6] == 28).all()
+    assert gat.shape == (2, 32)
+    assert list(gat[0, :8]) == [8, 128, 0, 10 * T, 0, 0, 1, 10 * T]
+    assert list(gat[1, :8]) == [5, 80, 0, T, 6 * T, 13 * T, 1, 8 * T]
+    for gi, frames in ((0, range(0, 8)), (1, range(8, 13))):
+        pieces = gat[gi, 8:8 + 3 * len(frames)].reshape(-1, 3)
+        assert [tuple(x) for x in pieces] == [(f, f * T + 3584, 16) for f in frames]
+    assert plan.info.n_units == 13 * 14 and plan.info.n_gathers == 2
 
 
 def test_segment_at_the_tile_pair_field_limit():
@@ -93,8 +142,9 @@ def test_plan_at_the_frame_limit():
     """The largest plan in frames (4096, the meta kernel's per-frame arrays), with
     16-token frames, window +-2 and reference frame 0. Expected values come from
     the window rule itself: per frame the clipped window [f-2, f+2] plus frame 0
-    when it lies outside; one segment and one 16-row tile per frame; units of one
-    cost class per key count."""
+    when it lies outside; one segment per frame. Each frame is a 16-row tail:
+    frames 8g..8g+7 share gathered tile g, over the union of their windows and
+    frame 0, and no segment keeps a tile of its own."""
     F, T, W, ref, bs = 4096, 16, 2, 0, 16
     plan = vd.attn_plan(F, T, W, ref, bs)
     frames = []
@@ -111,15 +161,17 @@ def test_plan_at_the_frame_limit():
     assert plan.info.live_pairs == sum(keys) * T
     assert plan.info.nnz == sum(keys) // bs
     segs = plan.segments().cpu().numpy()
-    units = plan.units().cpu().numpy().astype(np.int64)
-    assert plan.info.n_segments == F and len(units) == F
-    assert sorted(int(s[0]) for s in segs) == [f * T for f in range(F)]
-    # longest first: the unit key counts never increase, and each class has one count
-    ukeys = np.array([segs[u >> 16][7] for u in units])
-    assert (np.diff(ukeys) <= 0).all()
-    assert sorted(ukeys.tolist(), reverse=True) == sorted(keys, reverse=True)
-    cls = plan.class_offsets().cpu().numpy()
-    assert len(cls) - 1 == len(set(keys))
+    assert plan.info.n_segments == F
+    assert [int(s[0]) for s in segs] == [f * T for f in range(F)]
+    assert (segs[:, 6] == 0).all() and plan.info.n_units == 0 and plan.info.n_classes == 0
+    gat = plan.gathers().cpu().numpy()
+    assert gat.shape == (F // 8, 32)
+    for g in range(F // 8):
+        lo, hi = max(0, 8 * g - W), min(F - 1, 8 * g + 7 + W)
+        union = [0, (hi + 1) * T, 0, 0] if lo <= ref + 1 else [0, T, lo * T, (hi + 1) * T]
+        ukeys = (union[1] - union[0]) + (union[3] - union[2])
+        assert list(gat[g, :8]) == [8, 128] + union + [1, ukeys]
+        assert [tuple(x) for x in gat[g, 8:].reshape(-1, 3)] == [(f, f * T, 16) for f in range(8 * g, 8 * g + 8)]
 
 
 CENSUS = [
