@@ -74,7 +74,7 @@ __device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_fram
 // Union of a gathered tile's key runs r (empty runs have hi <= lo) with a
 // segment's runs s, written to u as at most two ascending runs; false when the
 // union needs more than two.
-__device__ bool union_runs(const int r[4], const int32_t *s, int u[4]) {
+__device__ bool union_runs(const int r[4], const int s[4], int u[4]) {
     int lo[4], hi[4], n = 0;
     for (int i = 0; i < 2; ++i) {
         if (r[2 * i + 1] > r[2 * i]) { lo[n] = r[2 * i]; hi[n] = r[2 * i + 1]; ++n; }
@@ -113,6 +113,7 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
     __shared__ int s_cnt[kMaxFrames];
     __shared__ int s_order[kMaxFrames];
     __shared__ int s_nused;   // entries of s_order that get units
+    __shared__ int s_pseg[kGatherMaxPieces], s_prows[kGatherMaxPieces];
     static_assert(kMaxFrames <= (1 << 12), "segment index field of s_order");
     for (int f = threadIdx.x; f < a.F; f += blockDim.x) {
         int r[4], live;
@@ -136,18 +137,69 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             long long per = a.T / a.bs;
             h.nnz = fp * per * per;
         }
-        // segments: consecutive frames with identical run lists --------------
+        // segments: consecutive frames with identical run lists, and gathered
+        // tiles ---------------------------------------------------------------
+        // A segment whose row count is not a multiple of 128 ends in a tile that
+        // holds only its last rows % 128 rows. Consecutive such tails (multiples
+        // of 16 rows, at most kGatherMaxRows each) are packed into one 128-row
+        // tile that visits the union of their key runs, when that union is at
+        // most two runs and at least a quarter smaller than the key runs the
+        // tails would each visit in a tile of their own; the segments then keep
+        // only their whole tiles. The gathered tiles are not work units: a second
+        // launch of the attention kernel runs them. Everything the packing reads
+        // is in registers or shared memory (s_pseg, s_prows: the open tile's
+        // pieces).
         int nseg = 0, cur[4] = {0, 0, 0, 0}, row0 = 0, rows = 0;
+        int ng = 0, npc = 0, grows = 0, gr[4] = {0, 0, 0, 0};
+        long long sum_keys = 0;
+        auto close = [&]() {
+            const long long ukeys = (long long)(gr[1] - gr[0]) + (gr[3] - gr[2]);
+            if (npc >= 2 && 4 * ukeys <= 3 * sum_keys) {
+                int32_t *rec = gathers + kGatherInts * ng;
+                rec[0] = npc; rec[1] = grows;
+                rec[2] = gr[0]; rec[3] = gr[1]; rec[4] = gr[2]; rec[5] = gr[3];
+                rec[6] = 1; rec[7] = (int)ukeys;
+                for (int k = 0; k < npc; ++k) {
+                    const int sg = s_pseg[k], nt = s_prows[k] / kTileRows;
+                    segments[kSegInts * sg + 6] = nt;
+                    s_order[sg] = (min((nt + kTilesPerUnit - 1) / kTilesPerUnit, kMaxPairsPerSegment) << 12) | sg;
+                }
+                ++ng;
+            }
+            npc = 0; grows = 0; sum_keys = 0;
+            gr[0] = gr[1] = gr[2] = gr[3] = 0;
+        };
+        auto add_tail = [&](int sg, int keys) {
+            const int tail = rows % kTileRows;
+            if (keys == 0 || tail == 0 || tail % 16 != 0 || tail > kGatherMaxRows) return;
+            int u[4];
+            const bool joins = union_runs(gr, cur, u) && npc < kGatherMaxPieces && grows + tail <= kTileRows;
+            if (npc > 0 && !joins) {
+                close();
+                union_runs(gr, cur, u);
+            }
+            int32_t *pc = gathers + kGatherInts * ng + kGatherPiece + 3 * npc;
+            pc[0] = sg; pc[1] = row0 + rows - tail; pc[2] = tail;
+            s_pseg[npc] = sg;
+            s_prows[npc] = rows;
+            gr[0] = u[0]; gr[1] = u[1]; gr[2] = u[2]; gr[3] = u[3];
+            grows += tail;
+            sum_keys += keys;
+            ++npc;
+        };
         auto flush = [&]() {
             int32_t *g = segments + kSegInts * nseg;
             const int ntile = (rows + kTileRows - 1) / kTileRows;
             const int keys = (cur[1] - cur[0]) + (cur[3] - cur[2]);
+            const int npairs = (ntile + kTilesPerUnit - 1) / kTilesPerUnit;
             g[0] = row0; g[1] = rows;
             g[2] = cur[0]; g[3] = cur[1]; g[4] = cur[2]; g[5] = cur[3];
             g[6] = ntile; g[7] = keys;
             // a unit code keeps the tile pair in its low 16 bits
-            if ((ntile + kTilesPerUnit - 1) / kTilesPerUnit > kMaxPairsPerSegment) h.error = 4;
+            if (npairs > kMaxPairsPerSegment) h.error = 4;
             s_cnt[nseg] = keys;        // frame counts are no longer needed
+            s_order[nseg] = (min(npairs, kMaxPairsPerSegment) << 12) | nseg;
+            add_tail(nseg, keys);
             ++nseg;
         };
         for (int f = 0; f < a.F; ++f) {
@@ -163,59 +215,8 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             rows = a.T;
         }
         flush();
-        if (h.error != 0) nseg = 0;
-        // gathered tiles -----------------------------------------------------
-        // A segment whose row count is not a multiple of 128 ends in a tile that
-        // holds only its last rows % 128 rows. Consecutive such tails (multiples
-        // of 16 rows, at most kGatherMaxRows each) are packed into one 128-row
-        // tile that visits the union of their key runs, when that union is at
-        // most two runs and at least a quarter smaller than the key runs the
-        // tails would each visit in a tile of their own; the segments then keep
-        // only their whole tiles. The gathered tiles are not work units: a second
-        // launch of the attention kernel runs them.
-        int ng = 0;
-        {
-            int np = 0, grows = 0, gr[4] = {0, 0, 0, 0};
-            long long sum_keys = 0;
-            auto close = [&]() {
-                int32_t *rec = gathers + kGatherInts * ng;
-                const long long ukeys = (long long)(gr[1] - gr[0]) + (gr[3] - gr[2]);
-                if (np >= 2 && 4 * ukeys <= 3 * sum_keys) {
-                    rec[0] = np; rec[1] = grows;
-                    rec[2] = gr[0]; rec[3] = gr[1]; rec[4] = gr[2]; rec[5] = gr[3];
-                    rec[6] = 1; rec[7] = (int)ukeys;
-                    for (int k = 0; k < np; ++k) {
-                        int32_t *g = segments + kSegInts * rec[kGatherPiece + 3 * k];
-                        g[6] = g[1] / kTileRows;
-                    }
-                    ++ng;
-                }
-                np = 0; grows = 0; sum_keys = 0;
-                gr[0] = gr[1] = gr[2] = gr[3] = 0;
-            };
-            for (int sg = 0; sg < nseg; ++sg) {
-                const int32_t *g = segments + kSegInts * sg;
-                const int tail = g[1] % kTileRows;
-                if (g[7] == 0 || tail == 0 || tail % 16 != 0 || tail > kGatherMaxRows) continue;
-                int u[4];
-                const bool joins = union_runs(gr, g + 2, u) && np < kGatherMaxPieces && grows + tail <= kTileRows;
-                if (np > 0 && !joins) {
-                    close();
-                    union_runs(gr, g + 2, u);
-                }
-                int32_t *pc = gathers + kGatherInts * ng + kGatherPiece + 3 * np;
-                pc[0] = sg; pc[1] = g[0] + g[1] - tail; pc[2] = tail;
-                gr[0] = u[0]; gr[1] = u[1]; gr[2] = u[2]; gr[3] = u[3];
-                grows += tail;
-                sum_keys += g[7];
-                ++np;
-            }
-            close();
-        }
-        for (int i = 0; i < nseg; ++i) {
-            const int npairs = (segments[kSegInts * i + 6] + kTilesPerUnit - 1) / kTilesPerUnit;
-            s_order[i] = (min(npairs, kMaxPairsPerSegment) << 12) | i;
-        }
+        close();
+        if (h.error != 0) nseg = ng = 0;
         // longest first (stable insertion sort on key count) ------------------
         for (int i = 1; i < nseg; ++i) {
             const int v = s_order[i], key = s_cnt[v & 0xFFF];
