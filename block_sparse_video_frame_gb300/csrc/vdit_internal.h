@@ -45,10 +45,12 @@ constexpr int kMaxFrames = 4096; // frames a plan may hold
 constexpr int kMaxClasses = 64;  // distinct unit costs a plan may hold
 constexpr int kMaxPairsPerSegment = 1 << 16;  // tile pairs a segment may hold (16-bit field)
 // Gathered tiles: the ragged last rows of several segments (each a multiple of
-// 16 rows, at most kGatherMaxRows) share one 128-row query tile. A record holds
-// its piece count, rows, the union of the pieces' key runs and the pieces.
+// 16 rows, at most kGatherMaxRows, of a segment of at least kGatherMinSegRows
+// rows) share one 128-row query tile. A record holds its piece count, rows, the
+// union of the pieces' key runs and the pieces.
 constexpr int kGatherMaxPieces = 8;
 constexpr int kGatherMaxRows = 64;
+constexpr int kGatherMinSegRows = 8 * kTileRows;
 constexpr int kGatherPiece = 8;                                  // first piece: seg, row0, rows
 constexpr int kGatherInts = kGatherPiece + 3 * kGatherMaxPieces; // ints per gathered-tile record
 

@@ -141,11 +141,13 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
         // tiles ---------------------------------------------------------------
         // A segment whose row count is not a multiple of 128 ends in a tile that
         // holds only its last rows % 128 rows. Consecutive such tails (multiples
-        // of 16 rows, at most kGatherMaxRows each) are packed into one 128-row
-        // tile that visits the union of their key runs, when that union is at
-        // most two runs and at least a quarter smaller than the key runs the
-        // tails would each visit in a tile of their own; the segments then keep
-        // only their whole tiles. The gathered tiles are not work units: a second
+        // of 16 rows, at most kGatherMaxRows each) of segments with at least 8
+        // whole tiles are packed into one 128-row tile that visits the union of
+        // their key runs, when that union is at most two runs and at least a
+        // quarter smaller than the key runs the tails would each visit in a tile
+        // of their own; the segments then keep only their whole tiles. (Shorter
+        // segments give a launch too little work to hide the gathered tiles,
+        // whose key runs are longer than any of theirs.) The gathered tiles are not work units: a second
         // launch of the attention kernel runs them. Everything the packing reads
         // is in registers or shared memory (s_pseg, s_prows: the open tile's
         // pieces).
@@ -171,7 +173,8 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
         };
         auto add_tail = [&](int sg, int keys) {
             const int tail = rows % kTileRows;
-            if (keys == 0 || tail == 0 || tail % 16 != 0 || tail > kGatherMaxRows) return;
+            if (keys == 0 || rows < kGatherMinSegRows || tail == 0 || tail % 16 != 0 || tail > kGatherMaxRows)
+                return;
             int u[4];
             const bool joins = union_runs(gr, cur, u) && npc < kGatherMaxPieces && grows + tail <= kTileRows;
             if (npc > 0 && !joins) {

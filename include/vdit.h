@@ -88,10 +88,11 @@ typedef struct {
     int32_t part;                /* VDIT_PART_*: the part of the mask this plan schedules */
     int32_t n_gathers;           /* gathered tiles per head: 128-row query tiles that hold
                                     the ragged last rows (rows % 128, a multiple of 16 up to
-                                    64) of two to eight segments and visit the union of their
-                                    key runs (at most two runs, at least a quarter fewer keys
-                                    than the tails would visit apart), masking each row to
-                                    its own runs; vdit_attn_fwd runs them in a second launch */
+                                    64) of two to eight segments of at least 1024 rows each
+                                    and visit the union of their key runs (at most two runs,
+                                    at least a quarter fewer keys than the tails would visit
+                                    apart), masking each row to its own runs; vdit_attn_fwd
+                                    runs them in a second launch */
     const int32_t *d_gathers;    /* [n_gathers][32]: pieces, rows, lo0, hi0, lo1, hi1 (the
                                     union), 1, keys, then per piece: segment, first row, rows */
 } vdit_plan_info;

@@ -34,6 +34,9 @@ CASES = [
     # 320 tokens: three 128-row tiles, so the last frame-blind block is a lone tile
     configs.Workload("lone_block", B=2, H=2, D=128, F=4, T=80, W=1, ref=2, block_size=16,
                      outlier_heads=(0,), seed=25),
+    # 1040-token frames: the window part's 16-row tails run as gathered tiles
+    configs.Workload("gather_parts", B=1, H=2, D=128, F=9, T=1040, W=2, ref=0, block_size=80,
+                     outlier_heads=(1,), seed=26),
 ]
 
 

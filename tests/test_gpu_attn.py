@@ -50,7 +50,17 @@ SMALL_CASES = [
                      outlier_heads=(), seed=20),
     configs.Workload("dense_n40", B=1, H=2, D=64, F=5, T=8, W=4, ref=0, block_size=16,
                      outlier_heads=(1,), seed=21),
+] + [
+    # frames of 8 whole tiles and a 16-, 48- or 64-row tail: the tails run as gathered
+    # tiles (eight, two and two to a tile) in the chained second launch
+    configs.Workload("gather_16", B=1, H=2, D=128, F=9, T=1040, W=1, ref=0, block_size=80,
+                     outlier_heads=(1,), seed=26),
+    configs.Workload("gather_48_d64", B=1, H=2, D=64, F=6, T=1072, W=2, ref=5, block_size=16,
+                     outlier_heads=(0,), seed=27),
+    configs.Workload("gather_64_noref", B=2, H=1, D=128, F=5, T=1088, W=1, ref=-1, block_size=64,
+                     outlier_heads=(), seed=28),
 ]
+GATHER_CASES = SMALL_CASES[-3:]
 
 
 def run_gpu(w, q, k, v, mode="auto", out_dtype=torch.float32, stats=None):
@@ -77,7 +87,7 @@ def test_attention_full_rows(w):
         assert elig[:, h].all() == (h not in w.outlier_heads)
 
 
-@pytest.mark.parametrize("w", SMALL_CASES[:3] + SMALL_CASES[5:7], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SMALL_CASES[:3] + SMALL_CASES[5:7] + GATHER_CASES, ids=lambda w: w.name)
 @pytest.mark.parametrize("mode", ["online", "static"])
 def test_forced_modes_agree(w, mode):
     """FORCE_ONLINE everywhere and FORCE_STATIC on eligible heads match the oracle."""

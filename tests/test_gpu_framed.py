@@ -23,6 +23,10 @@ CASES = [
                      outlier_heads=(1,), seed=22),
     configs.Workload("dense_small", B=1, H=3, D=64, F=5, T=48, W=4, ref=0, block_size=16,
                      outlier_heads=(2,), seed=23),
+    # 16-row tails in gathered tiles: each row takes its own segment's bound, and a
+    # tile takes the static path only if every piece's segment is eligible
+    configs.Workload("gather_outlier", B=1, H=3, D=128, F=9, T=1040, W=1, ref=0, block_size=80,
+                     outlier_heads=(1,), seed=24),
 ]
 
 

@@ -20,6 +20,7 @@ CASES = [
     (7, 16, 2, 3, 16), (6, 32, 0, -1, 32), (1, 64, 0, 0, 16), (8, 48, 1, 7, 16),
     (5, 24, 4, 0, 16), (12, 32, 3, -1, 16),
     (1, 1, 0, 0, 16), (5, 8, 4, 0, 16), (3, 5, 2, -1, 16),   # one token; tiny dense sequences
+    (9, 1040, 1, 0, 80), (6, 1072, 2, 5, 16), (5, 1088, 1, -1, 64),  # gathered tails of 16, 48, 64 rows
 ]
 
 
@@ -44,9 +45,9 @@ def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
     segments group frames with equal key runs; a gathered tile holds the ragged
     last rows of 2 to 8 segments (multiples of 16, at most 64 each, 128 in all)
     and visits the union of their key runs, at least a quarter smaller than the
-    runs the tails would each visit alone; the units (tile pairs of segments
-    that see keys) are ordered by non-increasing key count, one count per cost
-    class."""
+    runs the tails would each visit alone, and only segments of at least 1024
+    rows give up their tails; the units (tile pairs of segments that see keys)
+    are ordered by non-increasing key count, one count per cost class."""
     plan = vd.attn_plan(F, T, W, ref, bs)
     runs = plan.frame_runs().cpu().numpy()
     segs = plan.segments().cpu().numpy()
@@ -68,6 +69,7 @@ def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
             sg, r0, nr = (int(x) for x in g[8 + 3 * k:11 + 3 * k])
             s = segs[sg]
             assert nr == s[1] % 128 and nr % 16 == 0 and nr <= 64 and r0 == s[0] + s[1] - nr
+            assert s[1] >= 1024
             assert live[s[2]:s[3]].all() and live[s[4]:s[5]].all()
             covered[r0:r0 + nr] += 1
             total += nr
@@ -142,9 +144,9 @@ def test_plan_at_the_frame_limit():
     """The largest plan in frames (4096, the meta kernel's per-frame arrays), with
     16-token frames, window +-2 and reference frame 0. Expected values come from
     the window rule itself: per frame the clipped window [f-2, f+2] plus frame 0
-    when it lies outside; one segment per frame. Each frame is a 16-row tail:
-    frames 8g..8g+7 share gathered tile g, over the union of their windows and
-    frame 0, and no segment keeps a tile of its own."""
+    when it lies outside; one segment and one 16-row tile per frame (segments this
+    short keep their tails: no gathered tile); units of one cost class per key
+    count."""
     F, T, W, ref, bs = 4096, 16, 2, 0, 16
     plan = vd.attn_plan(F, T, W, ref, bs)
     frames = []
@@ -161,9 +163,26 @@ def test_plan_at_the_frame_limit():
     assert plan.info.live_pairs == sum(keys) * T
     assert plan.info.nnz == sum(keys) // bs
     segs = plan.segments().cpu().numpy()
-    assert plan.info.n_segments == F
-    assert [int(s[0]) for s in segs] == [f * T for f in range(F)]
-    assert (segs[:, 6] == 0).all() and plan.info.n_units == 0 and plan.info.n_classes == 0
+    units = plan.units().cpu().numpy().astype(np.int64)
+    assert plan.info.n_segments == F and len(units) == F and plan.info.n_gathers == 0
+    assert sorted(int(s[0]) for s in segs) == [f * T for f in range(F)]
+    # longest first: the unit key counts never increase, and each class has one count
+    ukeys = np.array([segs[u >> 16][7] for u in units])
+    assert (np.diff(ukeys) <= 0).all()
+    assert sorted(ukeys.tolist(), reverse=True) == sorted(keys, reverse=True)
+    cls = plan.class_offsets().cpu().numpy()
+    assert len(cls) - 1 == len(set(keys))
+
+
+def test_gathered_tiles_at_the_frame_limit():
+    """4096 frames of 1040 tokens (8 whole tiles and a 16-row tail each), window
+    +-2 and reference frame 0: frames 8g..8g+7 share gathered tile g, over the
+    union of their windows and frame 0, and every segment keeps its 8 tiles."""
+    F, T, W, ref, bs = 4096, 1040, 2, 0, 1040
+    plan = vd.attn_plan(F, T, W, ref, bs)
+    segs = plan.segments().cpu().numpy()
+    assert plan.info.n_segments == F and (segs[:, 6] == 8).all()
+    assert plan.info.n_units == 4 * F
     gat = plan.gathers().cpu().numpy()
     assert gat.shape == (F // 8, 32)
     for g in range(F // 8):
@@ -171,7 +190,8 @@ def test_plan_at_the_frame_limit():
         union = [0, (hi + 1) * T, 0, 0] if lo <= ref + 1 else [0, T, lo * T, (hi + 1) * T]
         ukeys = (union[1] - union[0]) + (union[3] - union[2])
         assert list(gat[g, :8]) == [8, 128] + union + [1, ukeys]
-        assert [tuple(x) for x in gat[g, 8:].reshape(-1, 3)] == [(f, f * T, 16) for f in range(8 * g, 8 * g + 8)]
+        want = [(f, f * T + 1024, 16) for f in range(8 * g, 8 * g + 8)]
+        assert [tuple(x) for x in gat[g, 8:].reshape(-1, 3)] == want
 
 
 CENSUS = [
