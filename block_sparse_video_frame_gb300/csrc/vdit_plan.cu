@@ -73,31 +73,40 @@ __device__ void frame_runs_of(const PlanArgs &a, int f, int r[4], int &live_fram
 
 // Union of a gathered tile's key runs r (empty runs have hi <= lo) with a
 // segment's runs s, written to u as at most two ascending runs; false when the
-// union needs more than two.
-__device__ bool union_runs(const int r[4], const int s[4], int u[4]) {
-    int lo[4], hi[4], n = 0;
-    for (int i = 0; i < 2; ++i) {
-        if (r[2 * i + 1] > r[2 * i]) { lo[n] = r[2 * i]; hi[n] = r[2 * i + 1]; ++n; }
-        if (s[2 * i + 1] > s[2 * i]) { lo[n] = s[2 * i]; hi[n] = s[2 * i + 1]; ++n; }
-    }
-    for (int i = 1; i < n; ++i)
-        for (int j = i; j > 0 && lo[j - 1] > lo[j]; --j) {
-            const int tl = lo[j], th = hi[j];
-            lo[j] = lo[j - 1]; hi[j] = hi[j - 1];
-            lo[j - 1] = tl; hi[j - 1] = th;
+// union needs more than two. Every index is fixed at compile time (a sorting
+// network, then an unrolled merge), so the arrays stay in registers.
+__device__ __forceinline__ bool union_runs(const int r[4], const int s[4], int u[4]) {
+    constexpr int kNone = 0x7fffffff;   // an empty run sorts last
+    int lo[4] = {r[0], r[2], s[0], s[2]}, hi[4] = {r[1], r[3], s[1], s[3]};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (hi[i] <= lo[i]) lo[i] = hi[i] = kNone;
+    auto cswap = [&](int i, int j) {
+        if (lo[j] < lo[i]) {
+            const int tl = lo[i], th = hi[i];
+            lo[i] = lo[j]; hi[i] = hi[j];
+            lo[j] = tl; hi[j] = th;
         }
-    int m = 0;
-    for (int i = 0; i < n; ++i) {
-        if (m > 0 && lo[i] <= hi[m - 1]) {
-            hi[m - 1] = max(hi[m - 1], hi[i]);
+    };
+    cswap(0, 1); cswap(2, 3); cswap(0, 2); cswap(1, 3); cswap(1, 2);
+    int m = 0, ml[2] = {0, 0}, mh[2] = {0, 0};
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (lo[i] == kNone) continue;
+        if (m > 0 && lo[i] <= (m == 1 ? mh[0] : mh[1])) {
+            if (m == 1) mh[0] = max(mh[0], hi[i]);
+            else mh[1] = max(mh[1], hi[i]);
+        } else if (m < 2) {
+            if (m == 0) { ml[0] = lo[i]; mh[0] = hi[i]; }
+            else { ml[1] = lo[i]; mh[1] = hi[i]; }
+            ++m;
         } else {
-            lo[m] = lo[i]; hi[m] = hi[i]; ++m;
+            ok = false;
         }
     }
-    if (m > 2) return false;
-    u[0] = m > 0 ? lo[0] : 0; u[1] = m > 0 ? hi[0] : 0;
-    u[2] = m > 1 ? lo[1] : 0; u[3] = m > 1 ? hi[1] : 0;
-    return true;
+    u[0] = ml[0]; u[1] = mh[0]; u[2] = ml[1]; u[3] = mh[1];
+    return ok;
 }
 
 // One block. The frames' runs are computed in parallel; one thread then builds
