@@ -221,7 +221,12 @@ VDIT_API vdit_status vdit_key_stats_noalloc(const void *q, const void *k, int32_
  * the plan's status word: the call itself returns before the kernel runs and
  * cannot report it, so check vdit_plan_status after the stream has passed the
  * call wherever a truncated result must not be used. The result is deterministic: two identical calls write
- * identical bytes. Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
+ * identical bytes. When the plan has gathered tiles (n_gathers > 0) the call
+ * makes two launches on `stream`: the tile pairs, then the gathered tiles as a
+ * programmatic dependent launch that may start while the first is still
+ * running and completes only after it; work the stream orders after the call
+ * follows both, and the pair can be captured in a CUDA graph.
+ * Errors: VDIT_ERR_INVALID, VDIT_ERR_UNSUPPORTED, VDIT_ERR_CUDA. */
 VDIT_API vdit_status vdit_attn_fwd(const vdit_plan *plan, const void *q, const void *k, const void *v,
                           void *o, int32_t o_dtype, float *lse, int32_t B, int32_t H, int32_t D,
                           const int64_t q_strides[3], const int64_t k_strides[3],
