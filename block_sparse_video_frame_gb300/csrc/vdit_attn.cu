@@ -249,11 +249,12 @@ __device__ __forceinline__ void decode_tiled(const Params &p, long long w, Work 
 }
 
 // Gathered tiles (the second launch): item w is record w % n_gathers of head
-// w / n_gathers. One query tile, whose rows come from up to 8 segments, over the
-// union of their key runs; with per-segment bounds it takes the static path only
-// if every piece's segment may.
+// B*H - 1 - w / n_gathers, last head first: the tile pairs end on the last heads,
+// whose K/V are then still in L2. One query tile, whose rows come from up to 8
+// segments, over the union of their key runs; with per-segment bounds it takes
+// the static path only if every piece's segment may.
 __device__ __forceinline__ void decode_gathered(const Params &p, long long w, Work &u) {
-    u.bh = (int)(w / p.n_gathers);
+    u.bh = p.B * p.H - 1 - (int)(w / p.n_gathers);
     u.gat = (int)(w % p.n_gathers);
     u.b = u.bh / p.H;
     u.h = u.bh % p.H;
@@ -769,7 +770,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if constexpr (kTiled || kGathered) {
                         const int kend = start + (kTiled ? kBK : nvalid);
                         const bool full = (rlo0 <= start && kend <= rhi0) || (rlo1 <= start && kend <= rhi1);
-                        const bool dead = kGathered && !(rlo0 < kend && start < rhi0) && !(rlo1 < kend && start < rhi1);
+                        const bool dead =
+                            kGathered && !(rlo0 < kend && start < rhi0) && !(rlo1 < kend && start < rhi1);
                         if (!__all_sync(0xffffffffu, full || dead)) {
 #pragma unroll
                             for (int e = 0; e < 128; ++e) {
@@ -829,7 +831,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     // no live key in this row yet (frame-blind tiling, gathered tile):
                     // every term is masked, any finite shift gives p = 0
-                    exps(v, dead ? INFINITY : (kTiled || kGathered) && mrun == -INFINITY ? 0.f : mrun);
+                    exps(v, dead ? INFINITY : ((kTiled || kGathered) && mrun == -INFINITY ? 0.f : mrun));
                     if (rescale) {
                         // O (after P.V of the previous key tile, which the S barrier of
                         // this tile covers) scaled to the new running max, before this
