@@ -175,6 +175,29 @@ def test_full_size_sampled_rows(w):
     assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
 
 
+def test_gathered_tiles_across_many_frames():
+    """512 frames of 1040 tokens, two heads (64 gathered tiles per head, 4096 tile
+    pairs): every tail row and the edges of 52 frames (the first two, the last two
+    and 48 seeded ones) against the oracle, in AUTO (head 1 online) and with the
+    per-segment bound."""
+    w = configs.Workload("gather_512", B=1, H=2, D=128, F=512, T=1040, W=2, ref=0, block_size=1040,
+                         outlier_heads=(1,), seed=29)
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    assert plan.info.n_gathers == 64 and plan.info.n_units == 4 * w.F
+    rng = np.random.default_rng(29)
+    frames = sorted(set([0, 1, w.F - 2, w.F - 1] + [int(x) for x in rng.choice(w.F, 48, replace=False)]))
+    rows = np.array([bh * w.N + f * w.T + i for bh in range(w.B * w.H) for f in frames
+                     for i in [0, 1023] + list(range(1024, w.T))], dtype=np.int64)
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v, rows)
+    qd, kd, vd_ = q.cuda(), k.cuda(), v.cuda()
+    for st in (vd.key_stats(qd, kd, w.scale), vd.key_stats_framed(plan, qd, kd, w.scale)):
+        o, lse = vd.attn_fwd(plan, qd, kd, vd_, st, w.scale, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check_close(gather_rows(o, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref,
+                    what="gather_512")
+
+
 def test_non_finite_scale_is_rejected():
     w = configs.TINY
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
