@@ -2,7 +2,9 @@
 workspace, attention) captured in a CUDA graph and replayed: every call is
 asynchronous and allocates nothing while it runs, so the step can be captured
 once and launched as one graph, and each replay writes the same bytes as the
-eager calls, also after the inputs change in place."""
+eager calls, also after the inputs change in place. The second geometry's
+attention call is two launches, the gathered tiles a programmatic dependent of
+the tile pairs, which the capture keeps as such."""
 import pytest
 import torch
 
@@ -12,10 +14,15 @@ from block_sparse_video_frame_gb300 import configs, synth
 pytestmark = pytest.mark.gpu
 
 
-def test_step_captured_in_a_cuda_graph_equals_eager():
-    w = configs.SMALL.with_(name="small_graph", H=4, outlier_heads=(3,))
+@pytest.mark.parametrize("w", [
+    configs.SMALL.with_(name="small_graph", H=4, outlier_heads=(3,)),
+    configs.Workload("gathered_graph", B=1, H=2, D=128, F=9, T=1040, W=1, ref=0, block_size=80,
+                     outlier_heads=(1,), seed=30),
+], ids=lambda w: w.name)
+def test_step_captured_in_a_cuda_graph_equals_eager(w):
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
     plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    assert (plan.info.n_gathers > 0) == (w.name == "gathered_graph")
     ws = torch.empty(max(16, vd.key_stats_workspace_bytes(w.B, w.H, w.N, w.D)), dtype=torch.uint8,
                      device="cuda")
     st = vd.key_stats(q, k, w.scale, workspace=ws)
