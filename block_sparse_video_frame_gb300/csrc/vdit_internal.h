@@ -51,6 +51,11 @@ constexpr int kMaxPairsPerSegment = 1 << 16;  // tile pairs a segment may hold (
 constexpr int kGatherMaxPieces = 8;
 constexpr int kGatherMaxRows = 64;
 constexpr int kGatherMinSegRows = 8 * kTileRows;
+// Tail tiles: a plan without gathered tiles, with at least kTailMinPairs tile
+// pairs per head, runs the tiles of its last kTailPairs pairs as one-piece
+// records in the same second launch.
+constexpr int kTailPairs = 8;
+constexpr int kTailMinPairs = 32;
 constexpr int kGatherPiece = 8;                                  // first piece: seg, row0, rows
 constexpr int kGatherInts = kGatherPiece + 3 * kGatherMaxPieces; // ints per gathered-tile record
 

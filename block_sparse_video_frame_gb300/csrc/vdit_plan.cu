@@ -239,6 +239,40 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
             }
             s_order[j + 1] = v;
         }
+        // tail tiles ---------------------------------------------------------
+        // A plan without gathered tiles hands the last kTailPairs tile pairs of
+        // its last segment in this order (the shortest units, which a launch runs
+        // last) to the chained second launch, as one-tile records of one piece
+        // each (the rows the tile owns). That launch's CTAs take the SMs the tile
+        // pairs free at their end one tile at a time. Only plans with at least
+        // kTailMinPairs tile pairs per head do this: a launch with less work has
+        // no long tail to fill.
+        if (ng == 0 && h.error == 0) {
+            int total = 0, last = -1;
+            for (int i = 0; i < nseg; ++i) {
+                const int v = s_order[i];
+                if (s_cnt[v & 0xFFF] == 0) break;
+                total += v >> 12;
+                if ((v >> 12) > 0) last = i;
+            }
+            if (last >= 0 && total >= kTailMinPairs) {
+                const int v = s_order[last], sg = v & 0xFFF, np = v >> 12;
+                const int mv = min(kTailPairs, np - 1);   // the segment keeps at least one pair
+                const int32_t *g = segments + kSegInts * sg;
+                const int srow0 = g[0], srows = g[1], ntile = g[6];
+                for (int t = 2 * (np - mv); t < ntile; ++t) {
+                    int32_t *rec = gathers + kGatherInts * ng;
+                    const int own = min(kTileRows, srows - kTileRows * t);
+                    rec[0] = 1; rec[1] = own;
+                    rec[2] = g[2]; rec[3] = g[3]; rec[4] = g[4]; rec[5] = g[5];
+                    rec[6] = 1; rec[7] = g[7];
+                    rec[kGatherPiece] = sg; rec[kGatherPiece + 1] = srow0 + kTileRows * t;
+                    rec[kGatherPiece + 2] = own;
+                    ++ng;
+                }
+                s_order[last] = ((np - mv) << 12) | sg;
+            }
+        }
         // cost classes and the first unit of each segment ---------------------
         int nu = 0, ncls = 0, prev_key = -1, i = 0;
         for (; i < nseg; ++i) {
@@ -431,8 +465,10 @@ vdit_status plan_create(int32_t F, int32_t T, int32_t W, int32_t ref, int32_t bs
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_segments), sizeof(int32_t) * kSegInts * F);
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_units), sizeof(int32_t) * p->units_cap);
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_class_off), sizeof(int32_t) * (kMaxClasses + 1));
-    // a gathered tile holds at least two segments' rows
-    if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_gathers), sizeof(int32_t) * kGatherInts * (F / 2 + 1));
+    // a gathered tile holds at least two segments' rows; or the plan has tail tiles
+    if (e == cudaSuccess)
+        e = device_alloc(reinterpret_cast<void **>(&p->d_gathers),
+                         sizeof(int32_t) * kGatherInts * (F / 2 + 1 + kTilesPerUnit * kTailPairs));
     if (e == cudaSuccess) e = device_alloc(reinterpret_cast<void **>(&p->d_status), sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) {

@@ -86,13 +86,17 @@ typedef struct {
     const int32_t *d_units;      /* [n_units]: (segment << 16) | tile pair, longest first */
     const int32_t *d_class_off;  /* [n_classes + 1] unit offsets of the cost classes */
     int32_t part;                /* VDIT_PART_*: the part of the mask this plan schedules */
-    int32_t n_gathers;           /* gathered tiles per head: 128-row query tiles that hold
-                                    the ragged last rows (rows % 128, a multiple of 16 up to
-                                    64) of two to eight segments of at least 1024 rows each
-                                    and visit the union of their key runs (at most two runs,
-                                    at least a quarter fewer keys than the tails would visit
-                                    apart), masking each row to its own runs; vdit_attn_fwd
-                                    runs them in a second launch */
+    int32_t n_gathers;           /* query tiles per head that vdit_attn_fwd runs in a second
+                                    launch: gathered tiles, which hold the ragged last rows
+                                    (rows % 128, a multiple of 16 up to 64) of two to eight
+                                    segments of at least 1024 rows each and visit the union
+                                    of their key runs (at most two runs, at least a quarter
+                                    fewer keys than the tails would visit apart), masking
+                                    each row to its own runs; or, in a plan without those and
+                                    with at least 32 tile pairs per head, tail tiles: the
+                                    tiles of the last 8 pairs of the last segment in unit
+                                    order, one record (one piece: the rows the tile owns)
+                                    each, no longer in d_units */
     const int32_t *d_gathers;    /* [n_gathers][32]: pieces, rows, lo0, hi0, lo1, hi1 (the
                                     union), 1, keys, then per piece: segment, first row, rows */
 } vdit_plan_info;

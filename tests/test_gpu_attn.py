@@ -198,6 +198,33 @@ def test_gathered_tiles_across_many_frames():
                     what="gather_512")
 
 
+@pytest.mark.parametrize("w", [
+    # dense, 65 tiles (the last owns 108 rows): tiles 50-64 become tail tiles
+    configs.Workload("tail_dense", B=1, H=2, D=128, F=5, T=1660, W=4, ref=0, block_size=16,
+                     outlier_heads=(1,), seed=31),
+    # 1080p-like frames: frame 0 (the shortest units) hands its tiles 48-63 over
+    configs.Workload("tail_sparse", B=1, H=2, D=128, F=4, T=8160, W=1, ref=0, block_size=240,
+                     outlier_heads=(0,), seed=32),
+], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", ["auto", "online"])
+def test_tail_tiles(w, mode):
+    """Plans without gathered tiles and with at least 32 tile pairs per head run the
+    tiles of their last 8 pairs as one-tile records in the second launch: every
+    row of those tiles, and stratified rows elsewhere, against the oracle."""
+    q, k, v = synth.make_qkv(w)
+    plan = vd.attn_plan(w.F, w.T, w.W, w.ref, w.block_size)
+    gat = plan.gathers().cpu().numpy()
+    assert len(gat) in (15, 16) and (gat[:, 0] == 1).all()
+    tail_rows = [bh * w.N + i for bh in range(w.B * w.H) for g in gat for i in range(g[9], g[9] + g[10])]
+    rows = np.unique(np.concatenate([np.array(tail_rows, dtype=np.int64), stratified_rows(w, per_frame_random=4)]))
+    o_ref, lse_ref, _ = oracle_rows(w, q, k, v, rows)
+    qd, kd, vd_ = q.cuda(), k.cuda(), v.cuda()
+    o, lse = vd.attn_fwd(plan, qd, kd, vd_, vd.key_stats(qd, kd, w.scale), w.scale, mode=mode,
+                         out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check_close(gather_rows(o, rows, w.N), o_ref, gather_rows(lse, rows, w.N), lse_ref, what=w.name)
+
+
 def test_non_finite_scale_is_rejected():
     w = configs.TINY
     q, k, v = (t.cuda() for t in synth.make_qkv(w))

@@ -41,13 +41,16 @@ def test_schedule_bit_exact(F, T, W, ref, bs):
 @pytest.mark.parametrize("F,T,W,ref,bs", CASES)
 def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
     """Host-logic check of the attention work list: every query row is owned by
-    exactly one 128-row tile, either a tile of its segment or a gathered tile;
-    segments group frames with equal key runs; a gathered tile holds the ragged
-    last rows of 2 to 8 segments (multiples of 16, at most 64 each, 128 in all)
-    and visits the union of their key runs, at least a quarter smaller than the
-    runs the tails would each visit alone, and only segments of at least 1024
-    rows give up their tails; the units (tile pairs of segments that see keys)
-    are ordered by non-increasing key count, one count per cost class."""
+    exactly one 128-row tile: a tile of a unit (a pair of its segment's tiles), a
+    gathered tile, or a tail tile. Segments group frames with equal key runs. A
+    gathered tile holds the ragged last rows of 2 to 8 segments (multiples of 16,
+    at most 64 each, 128 in all) and visits the union of their key runs, at least
+    a quarter smaller than the runs the tails would each visit alone; only
+    segments of at least 1024 rows give up their tails. A plan without gathered
+    tiles and with at least 32 tile pairs per head hands the tiles of the last 8
+    pairs of its last unit class's last segment to the second launch as one-tile
+    records. The units of a segment are its first tile pairs, ordered by
+    non-increasing key count, one count per cost class."""
     plan = vd.attn_plan(F, T, W, ref, bs)
     runs = plan.frame_runs().cpu().numpy()
     segs = plan.segments().cpu().numpy()
@@ -56,11 +59,26 @@ def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
     gat = plan.gathers().cpu().numpy()
     N = F * T
     covered = np.zeros(N, dtype=np.int64)
-    gathered_seg = set()
-    for gi, g in enumerate(gat):
+
+    def own(s, t):   # rows tile t of segment s owns (the last tile is shifted to end at the end)
+        row0, rows = int(s[0]), int(s[1])
+        return row0 + 128 * t, row0 + min(128 * (t + 1), rows)
+
+    gathered_seg, tail = set(), []
+    multi = [g for g in gat if g[0] >= 2]
+    for g in gat:
         npc, rows, lo0, hi0, lo1, hi1, one, keys = (int(x) for x in g[:8])
-        assert 2 <= npc <= 8 and one == 1 and 0 < rows <= 128
+        assert 1 <= npc <= 8 and one == 1 and 0 < rows <= 128
         assert keys == (hi0 - lo0) + (hi1 - lo1) and lo0 < hi0 and (hi1 == lo1 == 0 or hi0 < lo1 < hi1)
+        if npc == 1:   # a tail tile: one tile of a segment, the rows it owns
+            sg, r0, nr = (int(x) for x in g[8:11])
+            s = segs[sg]
+            t = (r0 - int(s[0])) // 128
+            assert len(multi) == 0 and (r0 - int(s[0])) % 128 == 0 and (r0, r0 + nr) == own(s, t)
+            assert [lo0, hi0, lo1, hi1] == [int(x) for x in s[2:6]] and keys == int(s[7])
+            covered[r0:r0 + nr] += 1
+            tail.append((sg, t))
+            continue
         live = np.zeros(N, dtype=bool)
         live[lo0:hi0] = True
         live[lo1:hi1] = True
@@ -82,19 +100,30 @@ def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
         for f in range(f0, f0 + rows // T):
             assert list(runs[f]) == [lo0, hi0, lo1, hi1]
         assert keys == (hi0 - lo0) + (hi1 - lo1)
-        if si in gathered_seg:
-            assert ntile == rows // 128
-            covered[row0:row0 + ntile * 128] += 1
-        else:
-            assert ntile == (rows + 127) // 128
-            covered[row0:row0 + rows] += 1
-    assert (covered == 1).all()
+        assert ntile == (rows // 128 if si in gathered_seg else (rows + 127) // 128)
     seen = {}
     for code in units:
         idx, pair = int(code) >> 16, int(code) & 0xFFFF
         seen[(idx, pair)] = seen.get((idx, pair), 0) + 1
-    want = {(si, p) for si, s in enumerate(segs) if s[7] > 0 for p in range((s[6] + 1) // 2)}
-    assert set(seen) == want and all(c == 1 for c in seen.values())
+        s = segs[idx]
+        for t in (2 * pair, 2 * pair + 1):
+            if t < s[6]:
+                lo, hi = own(s, t)
+                covered[lo:hi] += 1
+    assert all(c == 1 for c in seen.values())
+    assert (covered == 1).all()
+    # the units of a segment are its first tile pairs; the tail tiles are the rest of one segment
+    for si, s in enumerate(segs):
+        ps = sorted(p for (i, p) in seen if i == si)
+        assert ps == list(range(len(ps)))
+    if tail:
+        sg = tail[0][0]
+        ts = sorted(t for _, t in tail)
+        npairs = (int(segs[sg][6]) + 1) // 2
+        kept = len([1 for (i, _) in seen if i == sg])
+        assert all(x == sg for x, _ in tail) and ts == list(range(2 * kept, int(segs[sg][6])))
+        assert npairs - kept == min(8, npairs - 1) and len(units) + npairs - kept >= 32
+        assert units[-1] >> 16 == sg   # the last unit class's last segment
     keys = np.array([segs[int(c) >> 16][7] for c in units])
     assert (np.diff(keys) <= 0).all()
     assert cls[0] == 0 and cls[-1] == len(units)
@@ -123,15 +152,19 @@ def test_gathered_tiles_of_the_720p_geometry():
 
 def test_segment_at_the_tile_pair_field_limit():
     """Maximum size of the work-unit encoding (segment << 16 | tile pair): a
-    dense sequence of exactly 2^24 rows fills the 16-bit pair field with 65 536
-    pairs; one more 128-row tile is refused as unsupported instead of wrapping
-    into the segment field."""
+    dense sequence of exactly 2^24 rows holds 65 536 tile pairs in the 16-bit
+    pair field (the last 8 of them handed to the second launch as tail tiles);
+    one more 128-row tile is refused as unsupported instead of wrapping into the
+    segment field."""
     T = 1 << 24
     plan = vd.attn_plan(1, T, 0, 0, 4096)
     units = plan.units().cpu().numpy().astype(np.int64)
-    assert plan.info.n_segments == 1 and len(units) == 65536
+    # the last 8 pairs' 16 tiles run as tail tiles in the second launch
+    assert plan.info.n_segments == 1 and len(units) == 65536 - 8 and plan.info.n_gathers == 16
     assert (units >> 16 == 0).all()
-    assert np.array_equal(units & 0xFFFF, np.arange(65536))
+    assert np.array_equal(units & 0xFFFF, np.arange(65536 - 8))
+    gat = plan.gathers().cpu().numpy()
+    assert [int(g[9]) for g in gat] == [128 * t for t in range(2 * 65528, 2 * 65536)]
     assert plan.info.live_pairs == T * T
     plan.close()
     with pytest.raises(vd.VditError) as ei:
