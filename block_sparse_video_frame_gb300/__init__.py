@@ -259,9 +259,11 @@ class Plan:
         return self._device_array(self.info.d_class_off, self.info.n_classes + 1)
 
     def gathers(self):
-        """Gathered tiles, [n_gathers, 32] int32: pieces, rows, the union of the
-        pieces' key runs (lo0, hi0, lo1, hi1), 1, its key count, then per piece
-        (segment, first row, rows)."""
+        """Query tiles of the second attention launch, [n_gathers, 32] int32:
+        pieces, rows, the union of the pieces' key runs (lo0, hi0, lo1, hi1), 1,
+        its key count, then per piece (segment, first row, rows). Gathered tiles
+        hold the ragged tails of 2-8 segments; tail tiles (one piece) are the
+        tiles of the last tile pairs of a plan without gathered tiles."""
         return self._device_array(self.info.d_gathers, 32 * self.info.n_gathers).view(-1, 32)
 
     def close(self):
