@@ -36,9 +36,10 @@
 // their two running maxima first).
 // A segment whose rows are not a multiple of 128 leaves a short last tile. The
 // plan packs such tails of several segments into gathered tiles (each row masked
-// to its own key runs); a second instance of this kernel runs them, launched as
-// a programmatic dependent of the first so that its CTAs take the SMs the first
-// one's CTAs leave at its end.
+// to its own key runs), or, in a plan without those, hands the tiles of its last
+// tile pairs over as one-tile records ("tail tiles"); a second instance of this
+// kernel runs these records, launched as a programmatic dependent of the first
+// so that its CTAs take the SMs the first one's CTAs leave at its end.
 // Every wait is bounded in time; on expiry the CTA records a site code in the
 // plan's status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
