@@ -131,6 +131,110 @@ def test_work_units_cover_every_query_row_once(F, T, W, ref, bs):
         assert len(set(keys[a:b])) == 1
 
 
+def host_second_launch_records(F, T, W, ref):
+    """The records of the second attention launch, restated on the host from the
+    rule in vdit.h: segments are runs of frames with equal key runs; tails
+    (rows % 128, a multiple of 16, at most 64, of segments of at least 1024 rows
+    that see keys) are packed greedily in segment order into groups of at most 8
+    pieces and 128 rows whose key runs unite into at most two runs; a group of
+    two or more whose union has at most 3/4 of the pieces' keys is a gathered
+    tile. Without gathered tiles and with at least 32 tile pairs per head, the
+    tiles of the last 8 pairs (keeping one) of the last segment in unit order
+    (stable, by non-increasing key count) become one-piece tail tiles. Returns
+    the records as lists of 32 ints and the tile count of each segment."""
+    def runs_of(f):
+        lo, hi = max(0, f - W), min(F - 1, f + W)
+        r = [lo * T, (hi + 1) * T, 0, 0]
+        if ref >= 0 and not lo <= ref <= hi:
+            if ref == lo - 1:
+                r[0] = ref * T
+            elif ref == hi + 1:
+                r[1] = (ref + 1) * T
+            elif ref < lo:
+                r = [ref * T, (ref + 1) * T, lo * T, (hi + 1) * T]
+            else:
+                r = [lo * T, (hi + 1) * T, ref * T, (ref + 1) * T]
+        return r
+
+    segs = []                      # [row0, rows, runs]
+    for f in range(F):
+        r = runs_of(f)
+        if segs and segs[-1][2] == r:
+            segs[-1][1] += T
+        else:
+            segs.append([f * T, T, r])
+    ntile = [(rows + 127) // 128 for _, rows, _ in segs]
+    keys = [(r[1] - r[0]) + (r[3] - r[2]) for _, _, r in segs]
+
+    def union(a, b):
+        iv = sorted(x for x in [(a[0], a[1]), (a[2], a[3]), (b[0], b[1]), (b[2], b[3])] if x[1] > x[0])
+        m = []
+        for lo, hi in iv:
+            if m and lo <= m[-1][1]:
+                m[-1] = (m[-1][0], max(m[-1][1], hi))
+            else:
+                m.append((lo, hi))
+        if len(m) > 2:
+            return None
+        m += [(0, 0)] * (2 - len(m))
+        return [m[0][0], m[0][1], m[1][0], m[1][1]]
+
+    recs, group, gr, grows, gkeys = [], [], [0, 0, 0, 0], 0, 0
+
+    def close():
+        nonlocal group, gr, grows, gkeys
+        uk = (gr[1] - gr[0]) + (gr[3] - gr[2])
+        if len(group) >= 2 and 4 * uk <= 3 * gkeys:
+            rec = [len(group), grows] + gr + [1, uk]
+            for sg, r0, nr in group:
+                rec += [sg, r0, nr]
+                ntile[sg] = segs[sg][1] // 128
+            recs.append(rec + [0] * (32 - len(rec)))
+        group, gr, grows, gkeys = [], [0, 0, 0, 0], 0, 0
+
+    for sg, (row0, rows, r) in enumerate(segs):
+        tail = rows % 128
+        if keys[sg] == 0 or rows < 1024 or tail == 0 or tail % 16 or tail > 64:
+            continue
+        u = union(gr, r)
+        if group and not (u is not None and len(group) < 8 and grows + tail <= 128):
+            close()
+            u = union(gr, r)
+        group.append((sg, row0 + rows - tail, tail))
+        gr, grows, gkeys = u, grows + tail, gkeys + keys[sg]
+    close()
+    if not recs:
+        order = sorted(range(len(segs)), key=lambda i: -keys[i])   # stable
+        used = [i for i in order if keys[i] > 0]
+        pairs = [(ntile[i] + 1) // 2 for i in used]
+        if used and sum(pairs) >= 32:
+            sg = used[-1]
+            npairs = (ntile[sg] + 1) // 2
+            mv = min(8, npairs - 1)
+            row0, rows, r = segs[sg]
+            for t in range(2 * (npairs - mv), ntile[sg]):
+                own = min(128, rows - 128 * t)
+                rec = [1, own] + r + [1, keys[sg], sg, row0 + 128 * t, own]
+                recs.append(rec + [0] * (32 - len(rec)))
+    return recs, ntile
+
+
+@pytest.mark.parametrize("F,T,W,ref,bs", CASES + [(4096, 1040, 2, 0, 1040), (5, 1660, 4, 0, 16),
+                                                 (4, 8160, 1, 0, 240)])
+def test_second_launch_records_follow_the_rule(F, T, W, ref, bs):
+    """The device plan's gathered and tail tiles, and its segments' tile counts,
+    equal a host restatement of the packing rule, field by field."""
+    plan = vd.attn_plan(F, T, W, ref, bs)
+    want, ntile = host_second_launch_records(F, T, W, ref)
+    got = plan.gathers().cpu().numpy()
+    # fields past the pieces are not written by the plan: compare the used ones
+    assert len(got) == len(want)
+    for g, w in zip(got, want):
+        n = 8 + 3 * w[0]
+        assert [int(x) for x in g[:n]] == w[:n]
+    assert [int(x) for x in plan.segments().cpu().numpy()[:, 6]] == ntile
+
+
 def test_gathered_tiles_of_the_720p_geometry():
     """13 frames of 3600 tokens (28 whole tiles and a 16-row tail each), window
     +-2 and reference frame 0: the tails of frames 0-7 share one tile over frames
