@@ -156,10 +156,10 @@ __global__ void plan_meta_kernel(PlanArgs a, PlanHeader *__restrict__ hdr, int32
         // quarter smaller than the key runs the tails would each visit in a tile
         // of their own; the segments then keep only their whole tiles. (Shorter
         // segments give a launch too little work to hide the gathered tiles,
-        // whose key runs are longer than any of theirs.) The gathered tiles are not work units: a second
-        // launch of the attention kernel runs them. Everything the packing reads
-        // is in registers or shared memory (s_pseg, s_prows: the open tile's
-        // pieces).
+        // whose key runs are longer than any of theirs.) The gathered tiles are
+        // not work units: a second launch of the attention kernel runs them.
+        // Everything the packing reads is in registers or shared memory (s_pseg,
+        // s_prows: the open tile's pieces).
         int nseg = 0, cur[4] = {0, 0, 0, 0}, row0 = 0, rows = 0;
         int ng = 0, npc = 0, grows = 0, gr[4] = {0, 0, 0, 0};
         long long sum_keys = 0;
